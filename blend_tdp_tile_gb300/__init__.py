@@ -1,0 +1,268 @@
+"""GB300 Tiled Data Parallelism (TDP) tile split / blend -- Python binding.
+
+A thin ctypes layer over ``libtdp.so`` (the C ABI in ``include/tdp.h``): the
+functions here carry the C names, check that each torch tensor is a CUDA
+tensor of the size, dtype and contiguity the plan implies (so a wrong buffer
+is refused on the host instead of being overrun on the device), and pass raw
+pointers and the current CUDA stream through.  Every step of the path runs in
+the library's CUDA kernels; there is no fallback.  Importing this package
+loads ``libtdp.so`` and raises if it has not been built
+(``python blend_tdp_tile_gb300/build.py`` or ``__graft_entry__.build()``).
+
+Method: "Tiled Data Parallelism (TDP)" (LTX-2 docs, multigpu) -- split a
+patchified latent into overlapping (frames, height, width) tiles with their
+positions ("What it is"), normalise each tile's positions ("Position
+normalization"), filter conditioning tokens per tile ("Shared negative
+(reference) positions"), and blend the tile outputs with trapezoidal masks
+that sum to one ("What it is").
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+__all__ = [
+    "TDP_OK", "TDP_F32", "TDP_BF16", "TDP_MAX_TILES_PER_DIM", "TdpError",
+    "Plan", "tdp_plan_create", "tdp_plan_info", "tdp_plan_destroy",
+    "tdp_split", "tdp_norm_filter", "tdp_blend", "tdp_status_str", "tdp_last_error_detail",
+    "alloc_split_outputs", "alloc_filter_outputs", "LIB_PATH",
+]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtdp.so")
+
+TDP_OK = 0
+TDP_F32, TDP_BF16 = 0, 1
+TDP_MAX_TILES_PER_DIM = 64
+
+
+class TdpError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {tdp_status_str(status)} ({tdp_last_error_detail()})")
+
+
+class _DimCfg(ctypes.Structure):
+    _fields_ = [("num_tiles", ctypes.c_int32), ("overlap", ctypes.c_int32)]
+
+
+class _Problem(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("F", ctypes.c_int32), ("H", ctypes.c_int32),
+                ("W", ctypes.c_int32), ("C", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("dim", _DimCfg * 3)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is not built; run `python blend_tdp_tile_gb300/build.py` or __graft_entry__.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64p = ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(ctypes.c_int64)
+    lib.tdp_plan_create.argtypes = [ctypes.POINTER(_Problem), ctypes.POINTER(vp)]
+    lib.tdp_plan_create.restype = ctypes.c_int
+    lib.tdp_plan_info.argtypes = [vp, ctypes.POINTER(i32), i64p, vp, vp]
+    lib.tdp_plan_info.restype = ctypes.c_int
+    lib.tdp_plan_destroy.argtypes = [vp]
+    lib.tdp_plan_destroy.restype = None
+    lib.tdp_split.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp]
+    lib.tdp_split.restype = ctypes.c_int
+    lib.tdp_norm_filter.argtypes = [vp, vp, i32, vp, vp, i32, vp, vp, vp, vp, vp, vp]
+    lib.tdp_norm_filter.restype = ctypes.c_int
+    lib.tdp_blend.argtypes = [vp, vp, vp, vp]
+    lib.tdp_blend.restype = ctypes.c_int
+    lib.tdp_status_str.argtypes = [ctypes.c_int]
+    lib.tdp_status_str.restype = ctypes.c_char_p
+    lib.tdp_last_error_detail.argtypes = []
+    lib.tdp_last_error_detail.restype = ctypes.c_char_p
+    return lib
+
+
+_lib = _load()
+
+
+def tdp_status_str(status: int) -> str:
+    return _lib.tdp_status_str(int(status)).decode()
+
+
+def tdp_last_error_detail() -> str:
+    return _lib.tdp_last_error_detail().decode()
+
+
+def _check(status: int, where: str):
+    if status != TDP_OK:
+        raise TdpError(status, where)
+
+
+class Plan:
+    """Owning wrapper of a ``tdp_plan_t``; geometry read back through tdp_plan_info."""
+
+    def __init__(self, handle: int, problem: dict):
+        self._h = ctypes.c_void_p(handle)
+        self.problem = problem
+        n = ctypes.c_int32()
+        tot = ctypes.c_int64()
+        _check(_lib.tdp_plan_info(self._h, ctypes.byref(n), ctypes.byref(tot), None, None), "tdp_plan_info")
+        self.n_tiles = int(n.value)
+        self.total_tile_tokens = int(tot.value)
+        self.boxes = np.zeros((self.n_tiles, 3, 2), np.int32)
+        self.offsets = np.zeros(self.n_tiles + 1, np.int64)
+        _check(_lib.tdp_plan_info(self._h, None, None, self.boxes.ctypes.data_as(ctypes.c_void_p),
+                                  self.offsets.ctypes.data_as(ctypes.c_void_p)), "tdp_plan_info")
+        for k in ("B", "F", "H", "W", "C", "dtype"):
+            setattr(self, k, problem[k])
+
+    @property
+    def handle(self):
+        return self._h
+
+    @property
+    def esize(self):
+        return 4 if self.dtype == TDP_F32 else 2
+
+    def close(self):
+        if self._h is not None and self._h.value:
+            _lib.tdp_plan_destroy(self._h)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def tdp_plan_create(B, F, H, W, C, dtype, num_tiles, overlap) -> Plan:
+    """Validate a problem and compute its tiles (host only).  dtype: TDP_F32/TDP_BF16 or 'f32'/'bf16'."""
+    if isinstance(dtype, str):
+        dtype = {"f32": TDP_F32, "bf16": TDP_BF16}[dtype]
+    pr = _Problem()
+    pr.B, pr.F, pr.H, pr.W, pr.C, pr.dtype = B, F, H, W, C, dtype
+    for d in range(3):
+        pr.dim[d].num_tiles = int(num_tiles[d])
+        pr.dim[d].overlap = int(overlap[d])
+    h = ctypes.c_void_p()
+    _check(_lib.tdp_plan_create(ctypes.byref(pr), ctypes.byref(h)), "tdp_plan_create")
+    return Plan(h.value, dict(B=B, F=F, H=H, W=W, C=C, dtype=dtype,
+                              num_tiles=tuple(num_tiles), overlap=tuple(overlap)))
+
+
+def tdp_plan_info(plan: Plan):
+    """(n_tiles, total_tile_tokens, boxes[nt,3,2], offsets[nt+1])."""
+    return plan.n_tiles, plan.total_tile_tokens, plan.boxes.copy(), plan.offsets.copy()
+
+
+def tdp_plan_destroy(plan: Plan):
+    plan.close()
+
+
+# ------------------------------------------------------------------ marshalling
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t, name, numel, dtypes, align):
+    """Device pointer of a CUDA tensor after size/dtype/contiguity checks; None -> NULL."""
+    if t is None:
+        return None
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name}: dtype {t.dtype} not in {dtypes}")
+    if t.numel() != numel:
+        raise ValueError(f"{name}: {t.numel()} elements, expected {numel}")
+    p = t.data_ptr()
+    if p % align:
+        raise ValueError(f"{name}: not {align}-byte aligned")
+    return p
+
+
+def _latent_dtypes(plan):
+    torch = _torch()
+    return (torch.float32,) if plan.dtype == TDP_F32 else (torch.bfloat16,)
+
+
+def _stream(stream):
+    if stream is None:
+        return _torch().cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def tdp_split(plan: Plan, X, P, normalize, Y, Q, mn, mx, stream=None):
+    """Split X [B,F,H,W,C] (and positions P [B,3,T,2]) into tile-major Y (and Q, mn, mx)."""
+    torch = _torch()
+    B, T, C, nt, tot = plan.B, plan.F * plan.H * plan.W, plan.C, plan.n_tiles, plan.total_tile_tokens
+    lat = _latent_dtypes(plan)
+    args = (
+        _ptr(X, "X", B * T * C, lat, 16),
+        _ptr(P, "P", B * 3 * T * 2, (torch.int32,), 8),
+        int(bool(normalize)),
+        _ptr(Y, "Y", B * tot * C, lat, 16),
+        _ptr(Q, "Q", B * tot * 6, (torch.int32,), 8),
+        _ptr(mn, "mn", nt * B * 3, (torch.int32,), 4),
+        _ptr(mx, "mx", nt * B * 3, (torch.int32,), 4),
+        _stream(stream),
+    )
+    _check(_lib.tdp_split(plan.handle, *args), "tdp_split")
+
+
+def tdp_norm_filter(plan: Plan, K, N, mn, mx, normalize, keep, idx, count, kcount, Kout, stream=None):
+    """Per-tile keep / compaction / normalisation of conditioning tokens K [B,3,N,2]."""
+    torch = _torch()
+    B, nt = plan.B, plan.n_tiles
+    N = int(N)
+    i32 = (torch.int32,)
+    args = (
+        _ptr(K, "K", B * 3 * N * 2, i32, 8), N,
+        _ptr(mn, "mn", nt * B * 3, i32, 4),
+        _ptr(mx, "mx", nt * B * 3, i32, 4),
+        int(bool(normalize)),
+        _ptr(keep, "keep", nt * B * N, (torch.uint8,), 1),
+        _ptr(idx, "idx", nt * B * N, i32, 4),
+        _ptr(count, "count", nt * B, i32, 4),
+        _ptr(kcount, "kcount", B * N, i32, 4),
+        _ptr(Kout, "Kout", nt * B * 3 * N * 2, i32, 8),
+        _stream(stream),
+    )
+    _check(_lib.tdp_norm_filter(plan.handle, *args), "tdp_norm_filter")
+
+
+def tdp_blend(plan: Plan, Yout, Z, stream=None):
+    """Blend tile-major tile outputs Yout into Z [B,F,H,W,C] with the trapezoidal masks."""
+    B, T, C, tot = plan.B, plan.F * plan.H * plan.W, plan.C, plan.total_tile_tokens
+    lat = _latent_dtypes(plan)
+    _check(_lib.tdp_blend(plan.handle, _ptr(Yout, "Yout", B * tot * C, lat, 16),
+                          _ptr(Z, "Z", B * T * C, lat, 16), _stream(stream)), "tdp_blend")
+
+
+# ------------------------------------------------------------------ allocation helpers
+def alloc_split_outputs(plan: Plan, device="cuda", positions=True):
+    """Y [B*total, C], Q [B*total*6], mn, mx [nt,B,3] on `device` (torch allocations)."""
+    torch = _torch()
+    dt = torch.float32 if plan.dtype == TDP_F32 else torch.bfloat16
+    Y = torch.empty((plan.B * plan.total_tile_tokens, plan.C), dtype=dt, device=device)
+    if not positions:
+        return Y, None, None, None
+    Q = torch.empty(plan.B * plan.total_tile_tokens * 6, dtype=torch.int32, device=device)
+    mn = torch.empty((plan.n_tiles, plan.B, 3), dtype=torch.int32, device=device)
+    mx = torch.empty_like(mn)
+    return Y, Q, mn, mx
+
+
+def alloc_filter_outputs(plan: Plan, N: int, device="cuda"):
+    """keep, idx [nt,B,N], count [nt,B], kcount [B,N], Kout [nt,B,3,N,2]."""
+    torch = _torch()
+    nt, B = plan.n_tiles, plan.B
+    keep = torch.empty((nt, B, N), dtype=torch.uint8, device=device)
+    idx = torch.empty((nt, B, N), dtype=torch.int32, device=device)
+    count = torch.empty((nt, B), dtype=torch.int32, device=device)
+    kcount = torch.empty((B, N), dtype=torch.int32, device=device)
+    Kout = torch.empty((nt, B, 3, N, 2), dtype=torch.int32, device=device)
+    return keep, idx, count, kcount, Kout

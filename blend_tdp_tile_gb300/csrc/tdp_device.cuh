@@ -1,0 +1,137 @@
+// tdp_device.cuh -- device helpers shared by the TDP kernels: which tiles
+// cover a grid coordinate, their trapezoid-ramp weights, and the per-row
+// table of tile rows a latent row (b, f, h) maps to.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tdp_geom.h"
+
+// At most two tiles cover a coordinate along one dimension (neighbours
+// overlap by o and every core is at least o long).
+struct tdp_cover {
+    int32_t i0, i1;        // covering tiles, i0 < i1; i1 = -1 when only one
+    int32_t num0, num1;    // ramp numerators over den = o + 1
+};
+
+// Tiles covering coordinate x in [0, L) and their ramp numerators
+// ("Tiled Data Parallelism (TDP)", "What it is": trapezoidal masks summing to
+// one).  Across the o-cell overlap of tiles i, i+1, with k = x - lo[i+1], the
+// right tile weighs (k+1)/(o+1) and the left one (o-k)/(o+1).
+__device__ __forceinline__ tdp_cover tdp_cover_1d(const tdp_dim_geom &dg, int32_t x)
+{
+    // core index: the largest i with floor(i*L/n) <= x, i.e. ceil((x+1)*n/L) - 1
+    const int32_t ci = (int32_t)((((int64_t)x + 1) * dg.n + dg.L - 1) / dg.L) - 1;
+    tdp_cover c;
+    if (ci > 0 && x < dg.hi[ci - 1]) {
+        const int32_t k = x - dg.lo[ci];
+        c.i0 = ci - 1;
+        c.i1 = ci;
+        c.num0 = dg.o - k;
+        c.num1 = k + 1;
+    } else if (ci < dg.n - 1 && x >= dg.lo[ci + 1]) {
+        const int32_t k = x - dg.lo[ci + 1];
+        c.i0 = ci;
+        c.i1 = ci + 1;
+        c.num0 = dg.o - k;
+        c.num1 = k + 1;
+    } else {
+        c.i0 = ci;
+        c.i1 = -1;
+        c.num0 = dg.o + 1;
+        c.num1 = 0;
+    }
+    return c;
+}
+
+// fp32 ramp weight num/(o+1), IEEE round-to-nearest division.
+__device__ __forceinline__ float tdp_weight(int32_t num, int32_t o)
+{
+    return __fdiv_rn((float)num, (float)(o + 1));
+}
+
+// ---------------------------------------------------------------------------
+// Row table.  A latent row (b, f, h) lies in at most 2 F-tiles x 2 H-tiles
+// ("combos", in ascending (iF, iH)); inside each combo every W-tile iW holds a
+// contiguous run of that row.  For combo c and W-tile iW:
+//   tok[c][iW]  token index, in the tile-major buffers, of the row's cell w = 0
+//               (so cell w sits at tok + w; only w in [lo_W, hi_W) is used)
+//   qpos[c][iW] same for the tile-major position buffer, d = 0 (add d*T_t)
+//   Tt[c][iW]   tokens of the tile
+//   tb[c][iW]   t*B + b (row of mn/mx)
+// ---------------------------------------------------------------------------
+#define TDP_MAX_COMBOS 4
+
+struct tdp_row_combos {
+    int32_t nc;                           // combos (1, 2 or 4)
+    int32_t iF[TDP_MAX_COMBOS], iH[TDP_MAX_COMBOS];
+    float rFH[TDP_MAX_COMBOS];            // r_F * r_H of the combo
+};
+
+__device__ __forceinline__ tdp_row_combos tdp_make_combos(const tdp_geom &g, int32_t f, int32_t h)
+{
+    const tdp_cover cF = tdp_cover_1d(g.d[0], f);
+    const tdp_cover cH = tdp_cover_1d(g.d[1], h);
+    tdp_row_combos rc;
+    const int32_t nF = cF.i1 >= 0 ? 2 : 1, nH = cH.i1 >= 0 ? 2 : 1;
+    rc.nc = nF * nH;
+    int32_t c = 0;
+    for (int32_t a = 0; a < nF; ++a)
+        for (int32_t e = 0; e < nH; ++e, ++c) {
+            rc.iF[c] = a ? cF.i1 : cF.i0;
+            rc.iH[c] = e ? cH.i1 : cH.i0;
+            const float rF = tdp_weight(a ? cF.num1 : cF.num0, g.d[0].o);
+            const float rH = tdp_weight(e ? cH.num1 : cH.num0, g.d[1].o);
+            rc.rFH[c] = rF * rH;
+        }
+    return rc;
+}
+
+// Token offset off_t of tile (iF, iH, iW) in the tile-major buffers.
+__device__ __forceinline__ int64_t tdp_tile_off(const tdp_geom &g, int32_t iF, int32_t iH, int32_t iW)
+{
+    const int64_t SF = g.d[0].hi[iF] - g.d[0].lo[iF];
+    const int64_t SH = g.d[1].hi[iH] - g.d[1].lo[iH];
+    return (int64_t)g.d[0].pre[iF] * g.d[1].sum * g.d[2].sum +
+           SF * ((int64_t)g.d[1].pre[iH] * g.d[2].sum + SH * (int64_t)g.d[2].pre[iW]);
+}
+
+// Fill tok / qpos / Tt / tb (each [TDP_MAX_COMBOS * nW]) for row (b, f, h); entry c*nW + iW.
+// Called by the whole block; ends with __syncthreads().
+__device__ __forceinline__ void tdp_fill_row_table(const tdp_geom &g, const tdp_row_combos &rc,
+                                                   int32_t b, int32_t f, int32_t h,
+                                                   int64_t *tok, int64_t *qpos, int64_t *Tt,
+                                                   int32_t *tb)
+{
+    const int32_t nW = g.d[2].n;
+    for (int32_t e = threadIdx.x; e < rc.nc * nW; e += blockDim.x) {
+        const int32_t c = e / nW, iW = e % nW;
+        const int32_t iF = rc.iF[c], iH = rc.iH[c];
+        const int64_t SH = g.d[1].hi[iH] - g.d[1].lo[iH];
+        const int64_t SW = g.d[2].hi[iW] - g.d[2].lo[iW];
+        const int64_t SF = g.d[0].hi[iF] - g.d[0].lo[iF];
+        const int64_t T = SF * SH * SW;
+        const int64_t off = tdp_tile_off(g, iF, iH, iW);
+        const int64_t jrow = ((int64_t)(f - g.d[0].lo[iF]) * SH + (h - g.d[1].lo[iH])) * SW - g.d[2].lo[iW];
+        tok[e] = (int64_t)g.B * off + (int64_t)b * T + jrow;
+        if (qpos) qpos[e] = (int64_t)g.B * off * 3 + (int64_t)b * 3 * T + jrow;
+        if (Tt) Tt[e] = T;
+        if (tb) tb[e] = ((iF * g.d[1].n + iH) * nW + iW) * g.B + b;
+    }
+    __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// bf16 <-> fp32 on 16-byte vectors (8 bf16 or 4 fp32 per uint4).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float tdp_bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float tdp_bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+// Two fp32 -> packed bf16x2 (round to nearest even), low half = `lo`.
+__device__ __forceinline__ uint32_t tdp_pack_bf16x2(float lo, float hi)
+{
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}

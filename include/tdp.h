@@ -1,0 +1,208 @@
+/*
+ * tdp.h -- C ABI of the GB300 Tiled Data Parallelism (TDP) tile split / blend
+ * library (libtdp.so, sm_103a).
+ *
+ * Source of the method: "Tiled Data Parallelism (TDP)" (LTX-2 docs,
+ * multigpu).  The page's section "What it is" splits a patchified
+ * (frames, height, width) latent into overlapping tiles, runs the transformer
+ * per tile and blends the overlaps with trapezoidal masks that sum to one;
+ * "Position normalization" shifts each tile's positions so its generated
+ * tokens start at zero; "Shared negative (reference) positions" filters the
+ * conditioning tokens per tile; "API / Tiling config" gives per-dimension
+ * tile counts and overlaps.  On one GPU the page's cross-rank all_reduce of
+ * the blended tiles becomes an on-device accumulation over all tiles.
+ *
+ * Conventions shared by every entry point
+ *   - Dimensions are ordered (F, H, W) = (frames, height, width); d = 0 is time.
+ *   - Latent X and blended Z: [B, F, H, W, C], contiguous, C fastest.
+ *   - Generated-token positions P: [B, 3, T, 2] int32, T = F*H*W, token order
+ *     row-major (f, h, w), last axis = [start, end).
+ *   - Tiles are numbered t = (iF*nH + iH)*nW + iW; tokens inside a tile are
+ *     row-major over the tile's box.  Tile t holds T_t = SF*SH*SW tokens and
+ *     begins at token offset off_t = sum_{u<t} T_u (tdp_plan_info).
+ *   - Tile buffers are TILE-MAJOR so that each tile's input to the per-tile
+ *     transformer is one contiguous block:
+ *       Y (tiles, and tile outputs Yout): tile t = contiguous [B, T_t, C] at
+ *         element offset B*off_t*C;
+ *       Q (tile positions): tile t = contiguous [B, 3, T_t, 2] int32 at
+ *         element offset B*off_t*6.
+ *   - mn, mx: [n_tiles, B, 3] int32, the minimum start and maximum end of the
+ *     tile's generated-token positions (global coordinates).
+ *   - Every pointer argument named "device" must be device memory of the
+ *     current CUDA device; the caller allocates and owns every buffer and
+ *     the stream.  The library allocates no device memory.  Latent pointers
+ *     (X, Y, Yout, Z) must be 16-byte aligned and C*sizeof(element) must be a
+ *     multiple of 16; int32 buffers must be 4-byte aligned, Q and P 8-byte.
+ *   - Calls are asynchronous on `stream` (NULL = legacy default stream) and
+ *     validate their arguments on the host before any launch: an invalid
+ *     argument returns an error status and launches nothing.  A launch
+ *     failure returns TDP_ERR_CUDA; tdp_last_error_detail() then holds the
+ *     CUDA error string.  Faults inside a kernel surface on the stream's next
+ *     synchronisation, as for any CUDA work.  No C++ exception crosses the ABI.
+ *   - A plan is immutable once created and may be used concurrently from any
+ *     number of host threads and streams.
+ *   - Position arithmetic is int32 and wraps modulo 2^32.
+ */
+#ifndef TDP_H_
+#define TDP_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+struct CUstream_st;
+typedef struct CUstream_st *tdp_stream_t;
+
+typedef enum {
+    TDP_OK = 0,
+    TDP_ERR_INVALID_ARG = 1,       /* null pointer, negative size, bad enum value      */
+    TDP_ERR_BAD_GEOMETRY = 2,      /* tiling not valid for the latent extent           */
+    TDP_ERR_UNSUPPORTED_DTYPE = 3, /* dtype other than TDP_F32 / TDP_BF16              */
+    TDP_ERR_MISALIGNED = 4,        /* C*esize % 16 != 0 or a pointer misaligned        */
+    TDP_ERR_TOO_LARGE = 5,         /* beyond TDP_MAX_TILES_PER_DIM or index ranges     */
+    TDP_ERR_CUDA = 6               /* a CUDA runtime / launch error                    */
+} tdp_status;
+
+typedef enum { TDP_F32 = 0, TDP_BF16 = 1 } tdp_dtype;
+
+/* Most tiles along one dimension. */
+#define TDP_MAX_TILES_PER_DIM 64
+
+/* Per-dimension tiling: a tile COUNT and an overlap in latent grid units
+ * ("API / Tiling config": DimensionTilingConfig(num_tiles, overlap)). */
+typedef struct {
+    int32_t num_tiles;
+    int32_t overlap;
+} tdp_dim_cfg;
+
+/* One TDP problem: latent extent, channel count, storage type and the tiling
+ * of (F, H, W) (the page's TileCountConfig(frames, height, width)). */
+typedef struct {
+    int32_t B, F, H, W, C;
+    int32_t dtype;          /* tdp_dtype */
+    tdp_dim_cfg dim[3];     /* F, H, W */
+} tdp_problem;
+
+typedef struct tdp_plan_s *tdp_plan_t;   /* opaque, host-owned */
+
+/*
+ * tdp_plan_create -- validate a problem and compute its tile geometry.
+ * ("API / Tiling config": counts, not sizes; the box formula is not printed.)
+ *
+ * Boxes: along a dimension of extent L with n tiles and overlap o, the cores
+ * are c_i = floor(i*L/n), i = 0..n, and tile i spans
+ * [c_i - floor(o/2), c_{i+1} + (o - floor(o/2))), with no extension past 0
+ * or L; neighbours overlap by exactly o cells.  Valid when 1 <= n <= L,
+ * o >= 0 and, for n >= 2, floor(L/n) >= o (no cell lies in two overlaps);
+ * for n = 1 the overlap is ignored.  Also checks B >= 0, C >= 1, the dtype,
+ * C*esize % 16 == 0 and n <= TDP_MAX_TILES_PER_DIM, and that the 1-D masks of
+ * every dimension sum exactly to one (integer check).
+ *
+ *   prob  host pointer, read only during the call.
+ *   out   host pointer; receives a new plan on TDP_OK (unchanged otherwise).
+ * Host only: no CUDA call.  Release with tdp_plan_destroy.
+ */
+tdp_status tdp_plan_create(const tdp_problem *prob, tdp_plan_t *out);
+
+/*
+ * tdp_plan_info -- read a plan's geometry (host only).
+ *   n_tiles            out: number of tiles (may be NULL)
+ *   total_tile_tokens  out: sum_t T_t, tokens per batch item over all tiles (may be NULL)
+ *   boxes              out: [n_tiles][3][2] int32 [lo, hi) per dimension (may be NULL)
+ *   offsets            out: [n_tiles + 1] int64 token offsets off_t (may be NULL)
+ */
+tdp_status tdp_plan_info(tdp_plan_t plan, int32_t *n_tiles, int64_t *total_tile_tokens,
+                         int32_t *boxes, int64_t *offsets);
+
+/* Release a plan (NULL is ignored).  The caller must not use it afterwards. */
+void tdp_plan_destroy(tdp_plan_t plan);
+
+/*
+ * tdp_split -- tile split with tile positions and position normalisation.
+ * ("What it is": split the patchified latent into tiles, each tile's tokens
+ *  go to one transformer call; "Position normalization": each tile's
+ *  positions are shifted by the minimum start of its generated tokens, per
+ *  batch item and dimension, so they start at zero with widths kept.)
+ *
+ *   X          device [B,F,H,W,C] latent (dtype of the plan), read.
+ *   P          device [B,3,T,2] int32 generated-token positions, read; or NULL.
+ *   normalize  nonzero: Q holds positions minus mn (the page's default,
+ *              normalize_positions=True); zero: Q holds the global positions.
+ *   Y          device tile-major tiles, B * total_tile_tokens * C elements, written.
+ *   Q          device tile-major tile positions, B * total_tile_tokens * 6 int32,
+ *              written; NULL exactly when P is NULL.
+ *   mn, mx     device [n_tiles,B,3] int32, written: min start / max end over the
+ *              tile's generated tokens (global coordinates); NULL exactly when P is NULL.
+ *   stream     CUDA stream the work is queued on.
+ * Y[t][b][j][:] = X[b, lo_F+f, lo_H+h, lo_W+w, :] for tile-local token j = (f,h,w):
+ * a bit-exact copy.  Buffers must not overlap.
+ */
+tdp_status tdp_split(tdp_plan_t plan, const void *X, const int32_t *P, int32_t normalize,
+                     void *Y, int32_t *Q, int32_t *mn, int32_t *mx, tdp_stream_t stream);
+
+/*
+ * tdp_norm_filter -- per-tile conditioning-token filter with normalisation.
+ * ("Shared negative (reference) positions": conditioning tokens follow the
+ *  generated ones; a tile keeps a token whose [start,end) interval overlaps
+ *  the tile in all three dimensions, or whose time coordinate is negative;
+ *  a token kept by several tiles has blend weight 1/(tiles that kept it).
+ *  "Position normalization": kept tokens move by the tile's offset.)
+ *
+ * Tile extent in dimension d is [mn, mx) of its generated tokens; a token
+ * overlaps it when [max(s,mn), min(e,mx)) is non-empty; negative time means
+ * start_F < 0.  The test runs on global coordinates, per (tile, batch item).
+ *
+ *   K          device [B,3,N,2] int32 conditioning-token intervals, read.
+ *   N          tokens per batch item (>= 0; 0 writes only count and kcount-free zeros).
+ *   mn, mx     device [n_tiles,B,3] int32 from tdp_split, read.
+ *   normalize  nonzero: Kout = K - mn[t,b,d]; zero: Kout = K.
+ *   keep       device [n_tiles,B,N] uint8, written: 1 if tile t keeps token k of item b.
+ *   idx        device [n_tiles,B,N] int32, written: kept k in ascending order,
+ *              then -1 up to N.
+ *   count      device [n_tiles,B] int32, written: number of kept tokens.
+ *   kcount     device [B,N] int32, written: number of tiles that kept token k
+ *              (the denominator of the page's 1/(tiles that kept it) weight).
+ *   Kout       device [n_tiles,B,3,N,2] int32: entries [t,b,d,0:count) are the
+ *              kept tokens' intervals in idx order; entries past count are not written.
+ *   stream     CUDA stream.
+ */
+tdp_status tdp_norm_filter(tdp_plan_t plan, const int32_t *K, int32_t N,
+                           const int32_t *mn, const int32_t *mx, int32_t normalize,
+                           uint8_t *keep, int32_t *idx, int32_t *count, int32_t *kcount,
+                           int32_t *Kout, tdp_stream_t stream);
+
+/*
+ * tdp_blend -- mask-weighted accumulation of all tile outputs into the latent.
+ * ("What it is": overlapping regions are blended with trapezoidal masks and
+ *  the blended tiles are summed into the final result; the masks sum to 1.
+ *  The page sums ranks with one all_reduce; here every tile is on this GPU.)
+ *
+ * Mask of tile t at global cell (f,h,w): (r_F * r_H) * r_W, where along each
+ * dimension a tile weighs 1 inside its box, except across the o-cell overlap
+ * with a neighbour: with k = 0..o-1 from the overlap's left edge the right
+ * tile weighs (k+1)/(o+1) and the left tile (o-k)/(o+1).  Masks are computed
+ * in registers (fp32, IEEE division) and never stored.
+ * Z[b,f,h,w,:] = sum over the (at most 8) tiles covering the cell, in
+ * ascending t, of mask * Yout, accumulated in fp32 and stored in the plan's
+ * dtype (round to nearest even).
+ *
+ *   Yout   device tile-major tile outputs (same layout as tdp_split's Y), read.
+ *   Z      device [B,F,H,W,C] latent, written (every element).  Must not overlap Yout.
+ *   stream CUDA stream.
+ */
+tdp_status tdp_blend(tdp_plan_t plan, const void *Yout, void *Z, tdp_stream_t stream);
+
+/* Static string naming a status. */
+const char *tdp_status_str(tdp_status status);
+
+/* Detail of the last error returned on this host thread ("" if none). */
+const char *tdp_last_error_detail(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TDP_H_ */

@@ -1,0 +1,159 @@
+"""CPU-side checks of the C ABI: the library loads, exports every function the
+header declares, and its host-only plan logic agrees with the oracle and
+refuses invalid problems with the documented status (no GPU needed: plan
+creation makes no CUDA call)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wk
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _has_gpu():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
+# Tests that hand the library fake pointer values check that the host refuses them
+# before any launch; they run only where no GPU is present, so that a validation bug
+# can never turn into a kernel launch on a bogus address.
+no_gpu_only = pytest.mark.skipif(_has_gpu(), reason="fake-pointer checks run only without a GPU")
+
+
+@pytest.fixture(scope="module")
+def tdp():
+    import __graft_entry__
+    __graft_entry__.build()
+    import blend_tdp_tile_gb300
+    return blend_tdp_tile_gb300
+
+
+def _declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?[\w\s\*]+?\b(tdp_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for required in ("tdp_plan_create", "tdp_plan_info", "tdp_plan_destroy", "tdp_split",
+                     "tdp_norm_filter", "tdp_blend", "tdp_status_str"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(tdp):
+    lib = ctypes.CDLL(tdp.LIB_PATH)
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+
+
+@pytest.mark.parametrize("wl", wk.WORKLOADS, ids=lambda w: w.name)
+def test_plan_matches_oracle(tdp, wl):
+    plan = tdp.tdp_plan_create(wl.B, wl.F, wl.H, wl.W, wl.C, wl.dtype, wl.num_tiles, wl.overlap)
+    box, off = oracle.plan(oracle.problem_of(wl))
+    nt, tot, boxes, offsets = tdp.tdp_plan_info(plan)
+    assert nt == box.shape[0] and tot == off[-1]
+    assert np.array_equal(boxes, box) and np.array_equal(offsets, off)
+
+
+def test_plan_matches_oracle_sweep(tdp):
+    rng = np.random.default_rng(0)
+    for _ in range(300):
+        L = [int(rng.integers(1, 40)) for _ in range(3)]
+        n = [int(rng.integers(1, 7)) for _ in range(3)]
+        o = [int(rng.integers(0, 6)) for _ in range(3)]
+        try:
+            box, off = oracle.plan(oracle.problem(1, *L, 8, 4, n, o))
+        except ValueError:
+            with pytest.raises(tdp.TdpError) as ei:
+                tdp.tdp_plan_create(1, *L, 8, "f32", n, o)
+            assert ei.value.status in (2, 5)
+            continue
+        plan = tdp.tdp_plan_create(1, *L, 8, "f32", n, o)
+        assert np.array_equal(plan.boxes, box) and np.array_equal(plan.offsets, off)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(C=6, dtype="bf16"), 4),                      # 12-byte rows: not a multiple of 16
+    (dict(C=2, dtype="f32"), 4),
+    (dict(num_tiles=(1, 9, 1)), 2),                    # more tiles than cells
+    (dict(num_tiles=(1, 2, 2), overlap=(0, 5, 2)), 2),  # overlap longer than a core
+    (dict(overlap=(0, -1, 0)), 2),
+    (dict(num_tiles=(0, 1, 1)), 2),
+    (dict(W=200, num_tiles=(1, 1, 65), overlap=(0, 0, 0)), 5),
+    (dict(B=-1), 1),
+    (dict(F=0), 1),
+])
+def test_plan_rejects_invalid(tdp, kw, status):
+    base = dict(B=1, F=3, H=8, W=12, C=16, dtype="f32", num_tiles=(1, 2, 2), overlap=(0, 2, 2))
+    base.update(kw)
+    with pytest.raises(tdp.TdpError) as ei:
+        tdp.tdp_plan_create(base["B"], base["F"], base["H"], base["W"], base["C"], base["dtype"],
+                            base["num_tiles"], base["overlap"])
+    assert ei.value.status == status
+    assert tdp.tdp_last_error_detail()
+
+
+@no_gpu_only
+def test_bad_dtype_and_null_args(tdp):
+    lib = ctypes.CDLL(tdp.LIB_PATH)
+    pr = tdp._Problem()
+    pr.B, pr.F, pr.H, pr.W, pr.C, pr.dtype = 1, 3, 8, 12, 16, 7
+    for d in range(3):
+        pr.dim[d].num_tiles, pr.dim[d].overlap = 1, 0
+    h = ctypes.c_void_p()
+    lib.tdp_plan_create.argtypes = [ctypes.POINTER(tdp._Problem), ctypes.POINTER(ctypes.c_void_p)]
+    assert lib.tdp_plan_create(ctypes.byref(pr), ctypes.byref(h)) == 3
+    assert lib.tdp_plan_create(None, ctypes.byref(h)) == 1
+    lib.tdp_blend.argtypes = [ctypes.c_void_p] * 4
+    assert lib.tdp_blend(None, None, None, None) == 1
+    lib.tdp_split.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32] + [ctypes.c_void_p] * 5
+    assert lib.tdp_split(None, None, None, 1, None, None, None, None, None) == 1
+
+
+@no_gpu_only
+def test_host_validation_before_launch(tdp):
+    """Argument errors return a status without touching CUDA (runs without a GPU)."""
+    lib = ctypes.CDLL(tdp.LIB_PATH)
+    plan = tdp.tdp_plan_create(1, 3, 8, 12, 16, "f32", (1, 2, 2), (0, 2, 2))
+    vp = ctypes.c_void_p
+    lib.tdp_split.argtypes = [vp, vp, vp, ctypes.c_int32, vp, vp, vp, vp, vp]
+    lib.tdp_blend.argtypes = [vp, vp, vp, vp]
+    lib.tdp_norm_filter.argtypes = [vp, vp, ctypes.c_int32, vp, vp, ctypes.c_int32, vp, vp, vp, vp, vp, vp]
+    # positions half given
+    assert lib.tdp_split(plan.handle, 16, 8, 1, 16, None, None, None, None) == 1
+    # misaligned latent pointer (never dereferenced: refused on the host)
+    assert lib.tdp_split(plan.handle, 24, None, 1, 16, None, None, None, None) == 4
+    assert lib.tdp_blend(plan.handle, 16, 40, None) == 4
+    assert lib.tdp_blend(plan.handle, None, 16, None) == 1
+    assert lib.tdp_norm_filter(plan.handle, None, -1, 16, 16, 1, None, None, 16, None, None, None) == 1
+    assert lib.tdp_norm_filter(plan.handle, 8, 4, 16, 16, 1, 16, 16, 16, 16, 12, None) == 4
+
+
+def test_binding_refuses_wrong_sizes_on_host(tdp):
+    torch = pytest.importorskip("torch")
+    plan = tdp.tdp_plan_create(1, 3, 8, 12, 16, "f32", (1, 2, 2), (0, 2, 2))
+    with pytest.raises(ValueError):
+        tdp.tdp_blend(plan, torch.zeros(10), torch.zeros(10))   # CPU tensors are refused
+
+
+@no_gpu_only
+def test_zero_batch_is_a_no_op(tdp):
+    lib = ctypes.CDLL(tdp.LIB_PATH)
+    plan = tdp.tdp_plan_create(0, 3, 8, 12, 16, "f32", (1, 2, 2), (0, 2, 2))
+    vp = ctypes.c_void_p
+    lib.tdp_blend.argtypes = [vp, vp, vp, vp]
+    assert lib.tdp_blend(plan.handle, None, None, None) == 0

@@ -1,0 +1,214 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Split tiles, tile positions, position bounds, keep masks, compaction and
+counts are compared bit for bit; the blend within the stated tolerance of the
+fp64 oracle.  Source: "Tiled Data Parallelism (TDP)" (LTX-2 docs, multigpu).
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wk
+from gpu_path import (as_f64, assert_blend_close, assert_filter_equal, run_blend,
+                      run_split_filter, to_dev, to_host)
+
+pytestmark = pytest.mark.gpu
+
+FULL_ORACLE = ["tiny", "small", "medium", "temporal"]
+
+
+@pytest.fixture(scope="module")
+def tdp():
+    import __graft_entry__
+    __graft_entry__.build()
+    import blend_tdp_tile_gb300
+    return blend_tdp_tile_gb300
+
+
+def _plan(tdp, wl):
+    return tdp.tdp_plan_create(wl.B, wl.F, wl.H, wl.W, wl.C, wl.dtype, wl.num_tiles, wl.overlap)
+
+
+def _yout(wl, Y, seed):
+    """Stand-in transformer output: tile + N(0, sigma), in the storage type."""
+    noise = wk.make_noise(Y.shape, wl.sigma, np.random.default_rng(seed))
+    if wl.dtype == "f32":
+        return (Y + noise).astype(np.float32)
+    return wk.f32_to_bf16_bits(wk.bf16_bits_to_f32(Y) + noise)
+
+
+def _check_path(tdp, wl, X, P, K, normalize=True, stream=None):
+    plan = _plan(tdp, wl)
+    p = oracle.problem_of(wl)
+    out = run_split_filter(tdp, plan, wl, X, P, K, normalize=normalize, stream=stream)
+    Yref, Qref = oracle.split(p, X, P)
+    assert np.array_equal(out["Y"].reshape(Yref.shape), Yref), "tile split differs"
+    mn, mx = oracle.bounds(p, Qref)
+    assert np.array_equal(out["mn"], mn) and np.array_equal(out["mx"], mx)
+    Qn = oracle.normalize(p, Qref, mn) if normalize else Qref
+    assert np.array_equal(out["Q"], Qn), "tile positions differ"
+    ref = dict(zip(("keep", "idx", "count", "kcount", "Kout"), oracle.filter_cond(p, K, mn, mx, normalize)))
+    assert_filter_equal(out, ref, plan.n_tiles, wl.B)
+    # blend of noisy tile outputs
+    Yout = _yout(wl, Yref, wl.seed + 99)
+    Z = run_blend(tdp, plan, wl, Yout, stream=stream)
+    assert_blend_close(to_host(Z), oracle.blend(p, Yout), wl)
+    # reconstruction: tile outputs equal to their tiles give back the latent
+    Zr = to_host(run_blend(tdp, plan, wl, out["Yd"], stream=stream))
+    if wl.dtype == "bf16":
+        assert np.array_equal(Zr, X), "bf16 reconstruction is not bit-exact"
+    else:
+        assert np.allclose(Zr, X, rtol=1e-6, atol=1e-7)
+    return plan
+
+
+@pytest.mark.parametrize("name", FULL_ORACLE)
+def test_parity_workload(tdp, name):
+    wl = wk.by_name(name)
+    X, P, K = wk.make_inputs(wl)
+    _check_path(tdp, wl, X, P, K)
+
+
+@pytest.mark.parametrize("name", ["tiny", "temporal"])
+def test_parity_without_normalisation(tdp, name):
+    wl = wk.by_name(name)
+    X, P, K = wk.make_inputs(wl)
+    _check_path(tdp, wl, X, P, K, normalize=False)
+
+
+def test_parity_on_side_stream(tdp):
+    import torch
+    wl = wk.by_name("medium")
+    X, P, K = wk.make_inputs(wl)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        _check_path(tdp, wl, X, P, K, stream=s)
+
+
+def test_parity_edge_tokens(tdp):
+    """Conditioning intervals that end on, or start just below, every tile edge; plus
+    empty and inverted intervals."""
+    wl = wk.by_name("temporal").replace(F=12, H=30, W=27, C=16, n_cond=3000)
+    p = oracle.problem_of(wl)
+    box, _ = oracle.plan(p)
+    edges = [sorted(set(box[:, d, :].ravel().tolist())) for d in range(3)]
+    rng = np.random.default_rng(5)
+    X, P, _ = wk.make_inputs(wl)
+    K = wk.make_cond_positions(wl, rng, edges=edges, edge_frac=0.5)
+    K[:, 1, :40, 1] = K[:, 1, :40, 0]          # empty intervals
+    K[:, 2, 40:80, 1] = K[:, 2, 40:80, 0] - 3  # inverted intervals
+    _check_path(tdp, wl, X, P, K)
+
+
+def test_parity_wrapping_positions(tdp):
+    """Position values near the int32 limits: normalisation wraps the same way on both sides."""
+    wl = wk.by_name("tiny").replace(F=4, H=10, W=12, n_cond=64)
+    rng = np.random.default_rng(8)
+    X, _, K = wk.make_inputs(wl)
+    P = np.empty((wl.B, 3, wl.tokens, 2), np.int32)
+    P[..., 0] = rng.integers(-2**31, 2**31 - 1, size=P.shape[:-1], dtype=np.int64).astype(np.int32)
+    P[..., 1] = rng.integers(-2**31, 2**31 - 1, size=P.shape[:-1], dtype=np.int64).astype(np.int32)
+    K[..., 0] = rng.integers(-2**31, 2**31 - 1, size=K.shape[:-1], dtype=np.int64).astype(np.int32)
+    _check_path(tdp, wl, X, P, K)
+
+
+@pytest.mark.parametrize("shape", [
+    dict(num_tiles=(1, 1, 1), overlap=(0, 0, 0)),              # single tile: identity
+    dict(num_tiles=(2, 3, 4), overlap=(0, 0, 0)),              # zero overlap: permutation
+    dict(num_tiles=(2, 2, 2), overlap=(1, 1, 1)),              # odd overlap of one cell
+    dict(num_tiles=(3, 2, 3), overlap=(3, 5, 3)),              # odd overlaps, uneven cores
+    dict(H=32, W=40, num_tiles=(1, 2, 2), overlap=(0, 16, 20)),  # overlap == core: overlaps touch
+])
+def test_parity_geometries(tdp, shape):
+    base = wk.by_name("temporal").replace(F=9, H=26, W=30, C=24, n_cond=500)
+    wl = base.replace(**shape)
+    X, P, K = wk.make_inputs(wl)
+    _check_path(tdp, wl, X, P, K)
+
+
+def test_parity_max_tiles_per_dim(tdp):
+    wl = wk.by_name("tiny").replace(F=2, H=6, W=130, C=8, dtype="bf16",
+                                    num_tiles=(1, 3, 64), overlap=(0, 2, 1), n_cond=200)
+    X, P, K = wk.make_inputs(wl)
+    _check_path(tdp, wl, X, P, K)
+
+
+def test_parity_minimal_rows(tdp):
+    """16-byte tokens (bf16 C=8, fp32 C=4) and a one-cell-wide grid."""
+    for wl in (wk.by_name("tiny").replace(C=8, dtype="bf16"),
+               wk.by_name("tiny").replace(C=4),
+               wk.by_name("tiny").replace(F=1, H=1, W=1, num_tiles=(1, 1, 1), overlap=(0, 0, 0))):
+        X, P, K = wk.make_inputs(wl)
+        _check_path(tdp, wl, X, P, K)
+
+
+def test_no_cond_tokens(tdp):
+    wl = wk.by_name("small")
+    X, P, _ = wk.make_inputs(wl)
+    K = np.zeros((wl.B, 3, 0, 2), np.int32)
+    plan = _plan(tdp, wl)
+    out = run_split_filter(tdp, plan, wl, X, P, K)
+    assert (out["count"] == 0).all()
+
+
+def test_split_without_positions(tdp):
+    wl = wk.by_name("medium")
+    X, P, K = wk.make_inputs(wl)
+    plan = _plan(tdp, wl)
+    out = run_split_filter(tdp, plan, wl, X, P, K, positions=False)
+    Yref, _ = oracle.split(oracle.problem_of(wl), X, P)
+    assert np.array_equal(out["Y"].reshape(Yref.shape), Yref)
+
+
+def test_zero_batch(tdp):
+    import torch
+    wl = wk.by_name("tiny").replace(B=0)
+    plan = _plan(tdp, wl)
+    Y, Q, mn, mx = tdp.alloc_split_outputs(plan, "cuda")
+    X = torch.empty((0, wl.F, wl.H, wl.W, wl.C), device="cuda")
+    P = torch.empty((0, 3, wl.tokens, 2), dtype=torch.int32, device="cuda")
+    tdp.tdp_split(plan, X, P, 1, Y, Q, mn, mx)
+    Z = torch.empty_like(X)
+    tdp.tdp_blend(plan, Y, Z)
+    torch.cuda.synchronize()
+
+
+def test_large_workload_in_bench_configuration(tdp):
+    """The large workload at full size, as the benchmark launches it: split and filter
+    compared in full, the blend on sampled cells (each computed alone by the oracle) and
+    through the reconstruction property over every element."""
+    import torch
+    wl = wk.by_name("large")
+    X, P, K = wk.make_inputs(wl)
+    plan = _plan(tdp, wl)
+    p = oracle.problem_of(wl)
+    out = run_split_filter(tdp, plan, wl, X, P, K)
+    Yref, Qref = oracle.split(p, X, P)
+    assert np.array_equal(out["Y"].reshape(Yref.shape), Yref)
+    mn, mx = oracle.bounds(p, Qref)
+    assert np.array_equal(out["mn"], mn) and np.array_equal(out["mx"], mx)
+    assert np.array_equal(out["Q"], oracle.normalize(p, Qref, mn))
+    del Qref
+    ref = dict(zip(("keep", "idx", "count", "kcount", "Kout"), oracle.filter_cond(p, K, mn, mx, True)))
+    assert_filter_equal(out, ref, plan.n_tiles, wl.B)
+    # reconstruction over the whole latent
+    Zr = run_blend(tdp, plan, wl, out["Yd"])
+    assert torch.equal(Zr.view(torch.int16), to_dev(X).view(torch.int16))
+    del Zr
+    # noisy outputs, sampled cells: corners, tile edges and random cells
+    Yout = out["Yd"] + 0.05 * torch.randn(out["Yd"].shape, generator=torch.Generator("cuda").manual_seed(3),
+                                          device="cuda", dtype=torch.float32).to(torch.bfloat16)
+    Z = to_host(run_blend(tdp, plan, wl, Yout))
+    Yout_h = to_host(Yout)
+    rng = np.random.default_rng(4)
+    cells = [(0, 0, 0), (wl.F - 1, wl.H - 1, wl.W - 1)]
+    for d in range(3):
+        for v in np.unique(plan.boxes[:, d, :]):
+            c = [int(rng.integers(0, L)) for L in wl.dims]
+            c[d] = min(int(v), wl.dims[d] - 1)
+            cells.append(tuple(c))
+    cells += [tuple(int(rng.integers(0, L)) for L in wl.dims) for _ in range(300)]
+    for (f, h, w) in cells:
+        zc = oracle.blend_cell(p, Yout_h, 0, f, h, w)
+        assert_blend_close(Z[0, f, h, w], zc, wl)
+    assert np.isfinite(as_f64(Z)).all()

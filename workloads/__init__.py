@@ -98,9 +98,12 @@ def by_name(name: str) -> Workload:
 # --------------------------------------------------------------------------
 def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
     """Round float32 to bfloat16 (round to nearest, ties to even); uint16 bits."""
-    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    bias = ((u >> 16) & 1) + 0x7FFF
-    return ((u + bias) >> 16).astype(np.uint16)
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+    out = (u >> 16) & 1
+    out += 0x7FFF
+    out += u            # finite inputs only: wraps only for NaN/Inf bit patterns
+    out >>= 16
+    return out.astype(np.uint16)
 
 
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
