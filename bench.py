@@ -1,0 +1,446 @@
+#!/usr/bin/env python
+"""Benchmark of the TDP hot path: tile split (+positions) -> conditioning filter -> blend.
+
+One step = tdp_split, tdp_norm_filter and tdp_blend over the large workload
+(B=1, F=64, H=128, W=192, C=128 bf16; 2x8x8 tiles with overlap (4,16,16);
+16384 conditioning tokens), inputs resident in HBM.  The tile outputs fed to
+the blend are the split tiles plus N(0, 0.05) noise, made once before timing
+(the stand-in for the per-tile transformer, which is not part of the path).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  With torchrun (N > 1) every rank runs an independent
+replica of the step (the path has no exchange on one GPU); the value is the
+bytes of all ranks over the slowest rank's time.  --impl reference times the
+CPU oracle on this host instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import datetime
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as wk  # noqa: E402
+
+METRIC = "TDP split+blend effective GB/s (fraction of GB300 HBM peak); latent tokens/s"
+WORKLOAD = "large"
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+# ----------------------------------------------------------------------------- bytes
+def algorithmic_bytes(wl, total_tile_tokens, n_tiles, kept_total=None):
+    """Bytes each step must move at minimum (per batch of the workload).
+
+    split : read the latent once + write every tile token       (B*T*C*e + B*sumT*C*e)
+    pos   : read positions once + write tile positions           (B*T*24 + B*sumT*24)
+    filter: read cond tokens once, write keep/idx/kcount/count and the kept intervals
+    blend : read every tile-output token once + write the latent (B*sumT*C*e + B*T*C*e)
+    """
+    B, T, C, e = wl.B, wl.tokens, wl.C, wl.esize
+    tot = total_tile_tokens
+    N = wl.n_cond
+    split = B * T * C * e + B * tot * C * e
+    pos = B * T * 24 + B * tot * 24 + 2 * n_tiles * B * 3 * 4
+    kept = kept_total if kept_total is not None else 0
+    filt = B * N * 24 + n_tiles * B * N * (1 + 4) + n_tiles * B * 4 + B * N * 4 + kept * 24
+    blend = B * tot * C * e + B * T * C * e
+    return dict(split=split, pos=pos, filter=filt, blend=blend,
+                split_call=split + pos, step=split + pos + filt + blend)
+
+
+def config_of(wl, plan_tokens, n_tiles, parallelism):
+    return {
+        "workload": (f"{wl.name}: B={wl.B} F={wl.F} H={wl.H} W={wl.W} C={wl.C} {wl.dtype}, "
+                     f"tiles {'x'.join(map(str, wl.num_tiles))}, overlap {tuple(wl.overlap)}, "
+                     f"{n_tiles} tiles / {plan_tokens} tile tokens, {wl.n_cond} cond tokens"),
+        "parallelism": parallelism,
+        "l2": "inputs larger than L2 (tile outputs 1.27 GB, latent 0.40 GB per step); no flush",
+    }
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples every 200 ms (read-only query) while the timed region runs."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", gpu_id],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        rows = []
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t0 - 0.1 <= r[0] <= t1 + 0.1]
+        note = "samples inside the timed region"
+        if not inside:
+            inside, note = rows, "timed region shorter than the sampling period: samples of the whole run"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in inside for n, v in zip(names, r[3]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside), "note": note}
+
+
+def gpu_id_for_smi(torch, dev):
+    """nvidia-smi id (UUID when it can be matched) of the torch device."""
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        out = subprocess.run(["nvidia-smi", "--query-gpu=index,uuid", "--format=csv,noheader"],
+                             capture_output=True, text=True, timeout=20).stdout
+        for line in out.splitlines():
+            idx, u = [p.strip() for p in line.split(",")]
+            if uuid and (u.endswith(uuid) or uuid.endswith(u.replace("GPU-", ""))):
+                return u
+    except Exception:
+        pass
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    first = vis.split(",")[dev] if vis else str(dev)
+    return first.strip() or "0"
+
+
+# ----------------------------------------------------------------------------- peaks / traffic
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            return float(json.load(fh)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash(names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "blend_tdp_tile_gb300", "csrc", n), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {
+    "tdp_blend_kernel": ["tdp_blend.cu", "tdp_device.cuh", "tdp_geom.h"],
+    "tdp_split_kernel": ["tdp_split.cu", "tdp_device.cuh", "tdp_geom.h"],
+}
+
+
+def profiled_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None when the
+    kernel source changed since the capture (or none was taken)."""
+    try:
+        with open(PROFILE_TRAFFIC) as fh:
+            rec = json.load(fh)[kernel]
+    except Exception:
+        return None
+    if rec.get("source_hash") != kernel_source_hash(KERNEL_SOURCES[kernel]):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def oracle_step_time(wl, X, P, K):
+    """Wall time of one oracle pass (split, bounds, normalise, filter, blend) on one core."""
+    import oracle
+    p = oracle.problem_of(wl)
+    t = time.perf_counter()
+    Y, Q = oracle.split(p, X, P)
+    mn, mx = oracle.bounds(p, Q)
+    oracle.normalize(p, Q, mn)
+    keep, idx, count, kcount, Kout = oracle.filter_cond(p, K, mn, mx, True)
+    oracle.blend(p, Y)
+    return time.perf_counter() - t, int(count.sum())
+
+
+def cpu_baseline(wl, X, P, K, min_seconds=10.0, max_reps=20):
+    import oracle
+    oracle.build()
+    box, off = oracle.plan(oracle.problem_of(wl))
+    times, kept = [], 0
+    while (sum(times) < min_seconds and len(times) < max_reps) or not times:
+        dt, kept = oracle_step_time(wl, X, P, K)
+        times.append(dt)
+    ab = algorithmic_bytes(wl, int(off[-1]), box.shape[0], kept)["step"]
+    mean = sum(times) / len(times)
+    return {"value": ab / mean / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": (f"whole {wl.name} workload, {len(times)} passes ({sum(times):.1f} s), "
+                       f"single-threaded C oracle, fp64 blend"),
+            "s_per_step": mean}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import __graft_entry__
+    if rank == 0:
+        __graft_entry__.build()
+    if world > 1:
+        dist.barrier()
+    import blend_tdp_tile_gb300 as tdp
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    wl = wk.by_name(args.workload)
+    X, P, K = wk.make_inputs(wl)
+    plan = tdp.tdp_plan_create(wl.B, wl.F, wl.H, wl.W, wl.C, wl.dtype, wl.num_tiles, wl.overlap)
+    N = K.shape[2]
+    s = torch.cuda.Stream(device=dev)
+
+    def to_dev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(a).to(dev)
+
+    with torch.cuda.stream(s):
+        Xd, Pd, Kd = to_dev(X), to_dev(P), to_dev(K)
+        Y, Q, mn, mx = tdp.alloc_split_outputs(plan, dev)
+        keep, idx, count, kcount, Kout = tdp.alloc_filter_outputs(plan, N, dev)
+        Z = torch.empty_like(Xd)
+        tdp.tdp_split(plan, Xd, Pd, 1, Y, Q, mn, mx, stream=s)
+        gen = torch.Generator(device=dev).manual_seed(wl.seed + 7)
+        Yout = (Y.float() + wl.sigma * torch.randn(Y.shape, generator=gen, device=dev)).to(torch.bfloat16)
+    s.synchronize()
+
+    def step(evs=None):
+        if evs is not None:
+            evs[0].record(s)
+        tdp.tdp_split(plan, Xd, Pd, 1, Y, Q, mn, mx, stream=s)
+        if evs is not None:
+            evs[1].record(s)
+        tdp.tdp_norm_filter(plan, Kd, N, mn, mx, 1, keep, idx, count, kcount, Kout, stream=s)
+        if evs is not None:
+            evs[2].record(s)
+        tdp.tdp_blend(plan, Yout, Z, stream=s)
+        if evs is not None:
+            evs[3].record(s)
+
+    for _ in range(args.warmup):
+        step()
+    s.synchronize()
+    kept_total = int(count.sum().item())
+    ab = algorithmic_bytes(wl, plan.total_tile_tokens, plan.n_tiles, kept_total)
+
+    # ---- timed region: exactly K steps, barrier + synchronize on both sides
+    per = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(gpu_id_for_smi(torch, local_rank)) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    start.record(s)
+    for i in range(args.steps):
+        step(per[i])
+    stop.record(s)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if world > 1:
+        dist.barrier()
+    if sampler:
+        sampler.stop()
+    ms = start.elapsed_time(stop) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    k_ms = {
+        "split": statistics.mean(e[0].elapsed_time(e[1]) for e in per),
+        "norm_filter": statistics.mean(e[1].elapsed_time(e[2]) for e in per),
+        "blend": statistics.mean(e[2].elapsed_time(e[3]) for e in per),
+    }
+
+    # ---- end to end: host (pinned) buffers in, blended latent out, through the C ABI
+    e2e = None
+    if not args.no_e2e:
+        Xh = torch.from_numpy(X.view(np.int16)).pin_memory()
+        Ph = torch.from_numpy(P).pin_memory()
+        Kh = torch.from_numpy(K).pin_memory()
+        Zh = torch.empty(Xd.shape, dtype=torch.int16).pin_memory()
+
+        def e2e_step():
+            Xd.view(torch.int16).copy_(Xh, non_blocking=True)
+            Pd.copy_(Ph, non_blocking=True)
+            Kd.copy_(Kh, non_blocking=True)
+            step()
+            Zh.copy_(Z.view(torch.int16), non_blocking=True)
+
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                e2e_step()
+            s.synchronize()
+            if world > 1:
+                dist.barrier()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            for _ in range(args.e2e_steps):
+                e2e_step()
+            e1.record(s)
+            s.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": world * ab["step"] / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": X.nbytes + P.nbytes + K.nbytes, "d2h_bytes_per_step": X.nbytes,
+               "ms_per_step": e2e_ms, "steps": args.e2e_steps}
+
+    if rank != 0:
+        return None
+    peak, peak_kind = hbm_peak()
+    kern = {}
+    for name, b in (("split", ab["split_call"]), ("norm_filter", ab["filter"]), ("blend", ab["blend"])):
+        gbs = b / (k_ms[name] * 1e-3) / 1e9
+        kern[name] = {"ms": k_ms[name], "algorithmic_bytes": b, "GB/s": gbs, "frac": gbs / peak}
+    dom = "blend" if k_ms["blend"] >= k_ms["split"] else "split"
+    dom_kernel = "tdp_blend_kernel" if dom == "blend" else "tdp_split_kernel"
+    traffic = profiled_traffic(dom_kernel)
+    roof = {"bound": "hbm", "kernel": dom_kernel, "achieved": kern[dom]["GB/s"], "peak": peak,
+            "peak_kind": f"{peak_kind} copy bandwidth", "unit": "GB/s", "frac": kern[dom]["GB/s"] / peak,
+            "traffic": traffic, "algorithmic_bytes_per_launch": kern[dom]["algorithmic_bytes"]}
+    if dom == "split":
+        roof["note"] = "tdp_split timed as its three launches (bounds init, bounds, split)"
+    value = world * ab["step"] / (ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "dtype_detail": "bf16 latent storage, fp32 blend accumulation, int32 positions",
+        "data": "synthetic", "config": config_of(wl, plan.total_tile_tokens, plan.n_tiles,
+                                                 f"replicas x{world}" if world > 1 else "single GPU"),
+        "frac_of_peak": value / world / peak, "latent_tokens_per_s": world * wl.B * wl.tokens / (ms * 1e-3),
+        "step_algorithmic_bytes": ab["step"], "kernels": kern, "roofline": roof,
+        "gpu_launches": 5 * args.steps,
+        "clocks": sampler.summary(t0, t1) if sampler else None,
+        "e2e": e2e,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, X, P, K)
+    return line
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    """The CPU oracle, as it stands, on this host: K timed steps after W warm-ups, each step
+    a bounded sample of the large workload (its first Fs frames, same spatial tiling)."""
+    import oracle
+    oracle.build()
+    wl_full = wk.by_name(args.workload)
+    budget = 150.0 / max(1, args.steps + args.warmup)        # seconds per step
+    probe = wl_full.replace(F=8)
+    Xp, Pp, Kp = wk.make_inputs(probe)
+    t8, _ = oracle_step_time(probe, Xp, Pp, Kp)
+    Fs = int(min(wl_full.F, max(8, 8 * int(budget / max(t8, 1e-6)))))
+    wl = wl_full.replace(F=Fs) if Fs < wl_full.F else wl_full
+    X, P, K = wk.make_inputs(wl)
+    box, off = oracle.plan(oracle.problem_of(wl))
+    box_full, off_full = oracle.plan(oracle.problem_of(wl_full))
+    times, kept = [], 0
+    for _ in range(args.warmup):
+        oracle_step_time(wl, X, P, K)
+    for _ in range(args.steps):
+        dt, kept = oracle_step_time(wl, X, P, K)
+        times.append(dt)
+    ab = algorithmic_bytes(wl, int(off[-1]), box.shape[0], kept)["step"]
+    ms = 1e3 * sum(times) / len(times)
+    value = ab / (ms * 1e-3) / 1e9
+    sample = (f"{wl.name} workload cut to its first {wl.F} of {wl_full.F} frames (same H/W tiling, "
+              f"2 frame tiles) per step" if wl.F < wl_full.F else f"whole {wl.name} workload per step")
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(wl_full, int(off_full[-1]), box_full.shape[0], "host CPU, 1 thread"),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD, choices=[w.name for w in wk.WORKLOADS])
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    line = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
