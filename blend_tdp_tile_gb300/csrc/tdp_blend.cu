@@ -4,12 +4,15 @@
 // summed into the final result; the page's cross-rank all_reduce becomes,
 // with every tile on this GPU, one gather pass).
 //
-// Gather form: a block owns one latent row (b, f, h); every 16-byte output
-// vector reads its (at most 2 x 2 x 2) covering tile vectors, weights them with
-// masks computed in registers from the ramp formula, accumulates in fp32 in
-// ascending tile order and is stored once.  Each tile-output element is read
-// exactly once over the whole launch, each latent element written once, no
-// atomics and no scratch.
+// Gather form.  A block owns one latent row (b, f, h).  Once per row it builds
+// in shared memory the token offsets of the row inside every covering tile
+// (at most 2 F-tiles x 2 H-tiles = 4 "combos", times the W-tiles) and a table
+// of the (at most 2) W-tiles covering each cell with their ramp weights, so
+// the per-vector work is table lookups, at most 8 independent 16-byte loads
+// issued back to back, fp32 FMAs in ascending tile order and one streaming
+// store.  Every tile-output byte is read exactly once and every latent byte
+// written once: no atomics, no scratch memory, no inter-block waits.  At most
+// 64 registers per thread keep 32 warps, and so enough loads, in flight per SM.
 #include "tdp.h"
 #include "tdp_device.cuh"
 #include "tdp_internal.h"
@@ -17,27 +20,35 @@
 namespace {
 
 constexpr int kBlendThreads = 256;
-constexpr int kUnroll = 2;     // output vectors per thread in flight
+constexpr int kWTab = 1024;      // cells of the per-row W table built per pass
+
+// W-coverage of one cell: tiles iW0 (low 16 bits) and iW1 + 1 (high 16 bits,
+// 0 = none) and their ramp weights.
+struct __align__(16) tdp_wcell {
+    int32_t iw;
+    float r0, r1;
+    int32_t pad;
+};
 
 template <int BF16>
 struct vec_math;
 
 template <>
-struct vec_math<0> {           // 4 x fp32
+struct vec_math<0> {     // 4 x fp32
     static constexpr int kElems = 4;
-    __device__ static void fma(float (&acc)[4], float m, const uint4 &y)
+    __device__ static void mul(float (&a)[4], float m, const uint4 &y)
     {
-        acc[0] = fmaf(m, __uint_as_float(y.x), acc[0]);
-        acc[1] = fmaf(m, __uint_as_float(y.y), acc[1]);
-        acc[2] = fmaf(m, __uint_as_float(y.z), acc[2]);
-        acc[3] = fmaf(m, __uint_as_float(y.w), acc[3]);
+        a[0] = m * __uint_as_float(y.x);
+        a[1] = m * __uint_as_float(y.y);
+        a[2] = m * __uint_as_float(y.z);
+        a[3] = m * __uint_as_float(y.w);
     }
-    __device__ static void mul(float (&acc)[4], float m, const uint4 &y)
+    __device__ static void fma(float (&a)[4], float m, const uint4 &y)
     {
-        acc[0] = m * __uint_as_float(y.x);
-        acc[1] = m * __uint_as_float(y.y);
-        acc[2] = m * __uint_as_float(y.z);
-        acc[3] = m * __uint_as_float(y.w);
+        a[0] = fmaf(m, __uint_as_float(y.x), a[0]);
+        a[1] = fmaf(m, __uint_as_float(y.y), a[1]);
+        a[2] = fmaf(m, __uint_as_float(y.z), a[2]);
+        a[3] = fmaf(m, __uint_as_float(y.w), a[3]);
     }
     __device__ static uint4 pack(const float (&a)[4])
     {
@@ -47,24 +58,24 @@ struct vec_math<0> {           // 4 x fp32
 };
 
 template <>
-struct vec_math<1> {           // 8 x bf16
+struct vec_math<1> {     // 8 x bf16
     static constexpr int kElems = 8;
-    __device__ static void fma(float (&acc)[8], float m, const uint4 &y)
+    __device__ static void mul(float (&a)[8], float m, const uint4 &y)
     {
         const uint32_t w[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            acc[2 * i] = fmaf(m, tdp_bf16_lo(w[i]), acc[2 * i]);
-            acc[2 * i + 1] = fmaf(m, tdp_bf16_hi(w[i]), acc[2 * i + 1]);
+            a[2 * i] = m * tdp_bf16_lo(w[i]);
+            a[2 * i + 1] = m * tdp_bf16_hi(w[i]);
         }
     }
-    __device__ static void mul(float (&acc)[8], float m, const uint4 &y)
+    __device__ static void fma(float (&a)[8], float m, const uint4 &y)
     {
         const uint32_t w[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            acc[2 * i] = m * tdp_bf16_lo(w[i]);
-            acc[2 * i + 1] = m * tdp_bf16_hi(w[i]);
+            a[2 * i] = fmaf(m, tdp_bf16_lo(w[i]), a[2 * i]);
+            a[2 * i + 1] = fmaf(m, tdp_bf16_hi(w[i]), a[2 * i + 1]);
         }
     }
     __device__ static uint4 pack(const float (&a)[8])
@@ -75,65 +86,69 @@ struct vec_math<1> {           // 8 x bf16
 };
 
 template <int BF16>
-__global__ void __launch_bounds__(kBlendThreads)
-tdp_blend_kernel(const __grid_constant__ tdp_geom g, const uint4 *__restrict__ Yout, uint4 *__restrict__ Z)
+__global__ void __launch_bounds__(kBlendThreads, 4)
+tdp_blend_kernel(const __grid_constant__ tdp_geom g, int32_t cv_shift, const uint4 *__restrict__ Yout,
+                 uint4 *__restrict__ Z)
 {
     using VM = vec_math<BF16>;
     __shared__ int64_t s_tok[TDP_MAX_COMBOS * TDP_MAX_TILES_PER_DIM];
+    __shared__ tdp_wcell s_w[kWTab];
 
     const int32_t row = blockIdx.x;
     const int32_t h = row % g.H, f = (row / g.H) % g.F, b = row / (g.H * g.F);
     const tdp_row_combos rc = tdp_make_combos(g, f, h);
-    tdp_fill_row_table(g, rc, b, f, h, s_tok, nullptr, nullptr, nullptr);
+    tdp_fill_row_table(g, rc, b, f, h, s_tok, nullptr, nullptr, nullptr);   // ends with a barrier
 
-    const int32_t nW = g.d[2].n;
+    const int32_t nW = g.d[2].n, oW = g.d[2].o;
     const int32_t CV = (g.C * g.esize) >> 4;
-    const int32_t nvec = g.W * CV;
     const int64_t T = (int64_t)g.F * g.H * g.W;
-    uint4 *dst = Z + ((int64_t)b * T + ((int64_t)f * g.H + h) * g.W) * CV;
+    uint4 *zrow = Z + ((int64_t)b * T + ((int64_t)f * g.H + h) * g.W) * CV;
+    const int32_t nc = rc.nc;
+    float rFH[TDP_MAX_COMBOS];
+#pragma unroll
+    for (int c = 0; c < TDP_MAX_COMBOS; ++c) rFH[c] = c < nc ? rc.rFH[c] : 0.0f;
 
-    for (int32_t v0 = threadIdx.x; v0 < nvec; v0 += kUnroll * blockDim.x) {
-        // issue every load of kUnroll output vectors before any arithmetic
-        uint4 y[kUnroll][2 * TDP_MAX_COMBOS];
-        float m[kUnroll][2 * TDP_MAX_COMBOS];
-        int32_t nterm[kUnroll];
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int32_t v = v0 + u * blockDim.x;
-            nterm[u] = 0;
-            if (v >= nvec) continue;
-            const int32_t w = v / CV, cv = v - w * CV;
-            const tdp_cover cW = tdp_cover_1d(g.d[2], w);
-            const float rW0 = tdp_weight(cW.num0, g.d[2].o);
-            const float rW1 = tdp_weight(cW.num1, g.d[2].o);
+    for (int32_t wbase = 0; wbase < g.W; wbase += kWTab) {
+        const int32_t wn = min(kWTab, g.W - wbase);
+        for (int32_t i = threadIdx.x; i < wn; i += blockDim.x) {
+            const tdp_cover cW = tdp_cover_1d(g.d[2], wbase + i);
+            tdp_wcell e;
+            e.iw = cW.i0 | ((cW.i1 + 1) << 16);
+            e.r0 = tdp_weight(cW.num0, oW);
+            e.r1 = tdp_weight(cW.num1, oW);
+            e.pad = 0;
+            s_w[i] = e;
+        }
+        __syncthreads();
+        const int32_t nvec = wn * CV;
+        for (int32_t v = threadIdx.x; v < nvec; v += blockDim.x) {
+            const int32_t dw = cv_shift >= 0 ? (v >> cv_shift) : v / CV;
+            const int32_t cv = v - dw * CV;
+            const int32_t w = wbase + dw;
+            const tdp_wcell e = s_w[dw];
+            const int32_t iW0 = e.iw & 0xffff, iW1 = (e.iw >> 16) - 1;
+            // every load first (at most 8 in flight), then the arithmetic
+            uint4 y0[TDP_MAX_COMBOS], y1[TDP_MAX_COMBOS];
 #pragma unroll
             for (int c = 0; c < TDP_MAX_COMBOS; ++c) {
-                if (c < rc.nc) {
-                    y[u][2 * c] = __ldcs(Yout + (s_tok[c * nW + cW.i0] + w) * CV + cv);
-                    m[u][2 * c] = rc.rFH[c] * rW0;
-                    if (cW.i1 >= 0) {
-                        y[u][2 * c + 1] = __ldcs(Yout + (s_tok[c * nW + cW.i1] + w) * CV + cv);
-                        m[u][2 * c + 1] = rc.rFH[c] * rW1;
-                    }
+                if (c < nc) {
+                    y0[c] = __ldcs(Yout + (s_tok[c * nW + iW0] + w) * CV + cv);
+                    if (iW1 >= 0) y1[c] = __ldcs(Yout + (s_tok[c * nW + iW1] + w) * CV + cv);
                 }
             }
-            nterm[u] = cW.i1 >= 0 ? 2 : 1;
-        }
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            if (nterm[u] == 0) continue;
-            const int32_t v = v0 + u * blockDim.x;
             float acc[VM::kElems];
-            VM::mul(acc, m[u][0], y[u][0]);                   // first term sets the sign of zero
+            VM::mul(acc, rFH[0] * e.r0, y0[0]);          // the first term keeps the sign of zero
+            if (iW1 >= 0) VM::fma(acc, rFH[0] * e.r1, y1[0]);
 #pragma unroll
-            for (int c = 0; c < TDP_MAX_COMBOS; ++c) {
-                if (c < rc.nc) {
-                    if (c > 0) VM::fma(acc, m[u][2 * c], y[u][2 * c]);
-                    if (nterm[u] == 2) VM::fma(acc, m[u][2 * c + 1], y[u][2 * c + 1]);
+            for (int c = 1; c < TDP_MAX_COMBOS; ++c) {
+                if (c < nc) {
+                    VM::fma(acc, rFH[c] * e.r0, y0[c]);
+                    if (iW1 >= 0) VM::fma(acc, rFH[c] * e.r1, y1[c]);
                 }
             }
-            __stcs(dst + v, VM::pack(acc));
+            __stcs(zrow + (int64_t)w * CV + cv, VM::pack(acc));
         }
+        __syncthreads();   // the table is rebuilt for the next cells
     }
 }
 
@@ -147,14 +162,16 @@ extern "C" tdp_status tdp_blend(tdp_plan_t plan, const void *Yout, void *Z, tdp_
     if (!Yout || !Z) return tdp_fail(TDP_ERR_INVALID_ARG, "null Yout or Z");
     if (!tdp_aligned(Yout, 16) || !tdp_aligned(Z, 16))
         return tdp_fail(TDP_ERR_MISALIGNED, "Yout and Z must be 16-byte aligned");
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int32_t CV = (g.C * g.esize) >> 4;
+    const int32_t cv_shift = (CV & (CV - 1)) == 0 ? __builtin_ctz((unsigned)CV) : -1;
     const unsigned rows = (unsigned)((int64_t)g.B * g.F * g.H);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const uint4 *y = reinterpret_cast<const uint4 *>(Yout);
+    uint4 *z = reinterpret_cast<uint4 *>(Z);
     if (g.dtype == TDP_BF16)
-        tdp_blend_kernel<1><<<rows, kBlendThreads, 0, s>>>(g, reinterpret_cast<const uint4 *>(Yout),
-                                                           reinterpret_cast<uint4 *>(Z));
+        tdp_blend_kernel<1><<<rows, kBlendThreads, 0, s>>>(g, cv_shift, y, z);
     else
-        tdp_blend_kernel<0><<<rows, kBlendThreads, 0, s>>>(g, reinterpret_cast<const uint4 *>(Yout),
-                                                           reinterpret_cast<uint4 *>(Z));
+        tdp_blend_kernel<0><<<rows, kBlendThreads, 0, s>>>(g, cv_shift, y, z);
     const cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return tdp_fail(TDP_ERR_CUDA, cudaGetErrorString(err));
     return tdp_ok();

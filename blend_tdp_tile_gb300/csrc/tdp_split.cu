@@ -32,7 +32,10 @@ __global__ void tdp_bounds_init_kernel(int32_t *__restrict__ mn, int32_t *__rest
 }
 
 // Block (t, b, fl): the tile-local frame fl of tile t, batch item b.  Reduces all
-// three dimensions over the frame's SH x SW tokens, then 6 atomics.
+// three dimensions over the frame's SH x SW tokens (every thread keeps
+// 3 * kBoundsUnroll loads in flight), then 6 atomics.
+constexpr int kBoundsUnroll = 4;
+
 __global__ void __launch_bounds__(kBoundsThreads)
 tdp_bounds_kernel(const __grid_constant__ tdp_geom g, int32_t max_sf, const int2 *__restrict__ P,
                   int32_t *__restrict__ mn, int32_t *__restrict__ mx)
@@ -48,36 +51,54 @@ tdp_bounds_kernel(const __grid_constant__ tdp_geom g, int32_t max_sf, const int2
     const int32_t loW = g.d[2].lo[iW], SW = g.d[2].hi[iW] - loW;
     const int64_t T = (int64_t)g.F * g.H * g.W;
     const int32_t f = loF + fl;
+    const int2 *src0 = P + (int64_t)b * 3 * T + ((int64_t)f * g.H + loH) * g.W + loW;
 
+    int32_t lo[3] = {INT_MAX, INT_MAX, INT_MAX}, hi[3] = {INT_MIN, INT_MIN, INT_MIN};
+    const int32_t n = SH * SW;
+    for (int32_t e0 = threadIdx.x; e0 < n; e0 += kBoundsUnroll * blockDim.x) {
+        int2 v[kBoundsUnroll][3];
+#pragma unroll
+        for (int u = 0; u < kBoundsUnroll; ++u) {
+            const int32_t e = e0 + u * blockDim.x;
+            if (e < n) {
+                const int32_t hh = e / SW, ww = e - hh * SW;
+                const int64_t off = (int64_t)hh * g.W + ww;
+#pragma unroll
+                for (int d = 0; d < 3; ++d) v[u][d] = __ldg(src0 + d * T + off);
+            } else {
+#pragma unroll
+                for (int d = 0; d < 3; ++d) v[u][d] = make_int2(INT_MAX, INT_MIN);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kBoundsUnroll; ++u)
+#pragma unroll
+            for (int d = 0; d < 3; ++d) {
+                lo[d] = min(lo[d], v[u][d].x);
+                hi[d] = max(hi[d], v[u][d].y);
+            }
+    }
     __shared__ int32_t s_mn[3][kBoundsThreads / 32], s_mx[3][kBoundsThreads / 32];
     const int32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int32_t n = SH * SW;
-    for (int32_t d = 0; d < 3; ++d) {
-        const int2 *src = P + ((int64_t)b * 3 + d) * T + ((int64_t)f * g.H + loH) * g.W + loW;
-        int32_t lo = INT_MAX, hi = INT_MIN;
-        for (int32_t e = threadIdx.x; e < n; e += blockDim.x) {
-            const int32_t hh = e / SW, ww = e - hh * SW;
-            const int2 v = __ldg(src + (int64_t)hh * g.W + ww);
-            lo = min(lo, v.x);
-            hi = max(hi, v.y);
-        }
-        lo = __reduce_min_sync(0xffffffffu, lo);
-        hi = __reduce_max_sync(0xffffffffu, hi);
+#pragma unroll
+    for (int d = 0; d < 3; ++d) {
+        const int32_t a = __reduce_min_sync(0xffffffffu, lo[d]);
+        const int32_t z = __reduce_max_sync(0xffffffffu, hi[d]);
         if (lane == 0) {
-            s_mn[d][warp] = lo;
-            s_mx[d][warp] = hi;
+            s_mn[d][warp] = a;
+            s_mx[d][warp] = z;
         }
     }
     __syncthreads();
     if (threadIdx.x < 3) {
         const int32_t d = threadIdx.x;
-        int32_t lo = INT_MAX, hi = INT_MIN;
+        int32_t a = INT_MAX, z = INT_MIN;
         for (int32_t w = 0; w < kBoundsThreads / 32; ++w) {
-            lo = min(lo, s_mn[d][w]);
-            hi = max(hi, s_mx[d][w]);
+            a = min(a, s_mn[d][w]);
+            z = max(z, s_mx[d][w]);
         }
-        atomicMin(mn + (int64_t)tb * 3 + d, lo);
-        atomicMax(mx + (int64_t)tb * 3 + d, hi);
+        atomicMin(mn + (int64_t)tb * 3 + d, a);
+        atomicMax(mx + (int64_t)tb * 3 + d, z);
     }
 }
 

@@ -156,7 +156,7 @@ tdp_status tdp_split(tdp_plan_t plan, const void *X, const int32_t *P, int32_t n
  * start_F < 0.  The test runs on global coordinates, per (tile, batch item).
  *
  *   K          device [B,3,N,2] int32 conditioning-token intervals, read.
- *   N          tokens per batch item (>= 0; 0 writes only count and kcount-free zeros).
+ *   N          tokens per batch item (>= 0; with N = 0 only count is written, all zero).
  *   mn, mx     device [n_tiles,B,3] int32 from tdp_split, read.
  *   normalize  nonzero: Kout = K - mn[t,b,d]; zero: Kout = K.
  *   keep       device [n_tiles,B,N] uint8, written: 1 if tile t keeps token k of item b.
