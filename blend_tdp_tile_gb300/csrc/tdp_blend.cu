@@ -93,6 +93,11 @@ tdp_blend_kernel(const __grid_constant__ tdp_geom g, int32_t cv_shift, const uin
     using VM = vec_math<BF16>;
     __shared__ int64_t s_tok[TDP_MAX_COMBOS * TDP_MAX_TILES_PER_DIM];
     __shared__ tdp_wcell s_w[kWTab];
+    __shared__ int32_t s_loW[TDP_MAX_TILES_PER_DIM], s_hiW[TDP_MAX_TILES_PER_DIM];
+    for (int32_t i = threadIdx.x; i < g.d[2].n; i += blockDim.x) {
+        s_loW[i] = g.d[2].lo[i];
+        s_hiW[i] = g.d[2].hi[i];
+    }
 
     const int32_t row = blockIdx.x;
     const int32_t h = row % g.H, f = (row / g.H) % g.F, b = row / (g.H * g.F);
@@ -111,7 +116,7 @@ tdp_blend_kernel(const __grid_constant__ tdp_geom g, int32_t cv_shift, const uin
     for (int32_t wbase = 0; wbase < g.W; wbase += kWTab) {
         const int32_t wn = min(kWTab, g.W - wbase);
         for (int32_t i = threadIdx.x; i < wn; i += blockDim.x) {
-            const tdp_cover cW = tdp_cover_1d(g.d[2], wbase + i);
+            const tdp_cover cW = tdp_cover_tab(s_loW, s_hiW, nW, g.W, oW, wbase + i);
             tdp_wcell e;
             e.iw = cW.i0 | ((cW.i1 + 1) << 16);
             e.r0 = tdp_weight(cW.num0, oW);

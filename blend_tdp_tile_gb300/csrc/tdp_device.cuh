@@ -19,31 +19,39 @@ struct tdp_cover {
 // Tiles covering coordinate x in [0, L) and their ramp numerators
 // ("Tiled Data Parallelism (TDP)", "What it is": trapezoidal masks summing to
 // one).  Across the o-cell overlap of tiles i, i+1, with k = x - lo[i+1], the
-// right tile weighs (k+1)/(o+1) and the left one (o-k)/(o+1).
-__device__ __forceinline__ tdp_cover tdp_cover_1d(const tdp_dim_geom &dg, int32_t x)
+// right tile weighs (k+1)/(o+1) and the left one (o-k)/(o+1).  lo/hi may live in
+// shared memory (lanes with different x then read them in parallel) or in the
+// kernel parameters.  32-bit arithmetic: the plan keeps L * (n + 1) below 2^32.
+__device__ __forceinline__ tdp_cover tdp_cover_tab(const int32_t *lo, const int32_t *hi, int32_t n, int32_t L,
+                                                   int32_t o, int32_t x)
 {
     // core index: the largest i with floor(i*L/n) <= x, i.e. ceil((x+1)*n/L) - 1
-    const int32_t ci = (int32_t)((((int64_t)x + 1) * dg.n + dg.L - 1) / dg.L) - 1;
+    const int32_t ci = (int32_t)(((uint32_t)(x + 1) * (uint32_t)n + (uint32_t)(L - 1)) / (uint32_t)L) - 1;
     tdp_cover c;
-    if (ci > 0 && x < dg.hi[ci - 1]) {
-        const int32_t k = x - dg.lo[ci];
+    if (ci > 0 && x < hi[ci - 1]) {
+        const int32_t k = x - lo[ci];
         c.i0 = ci - 1;
         c.i1 = ci;
-        c.num0 = dg.o - k;
+        c.num0 = o - k;
         c.num1 = k + 1;
-    } else if (ci < dg.n - 1 && x >= dg.lo[ci + 1]) {
-        const int32_t k = x - dg.lo[ci + 1];
+    } else if (ci < n - 1 && x >= lo[ci + 1]) {
+        const int32_t k = x - lo[ci + 1];
         c.i0 = ci;
         c.i1 = ci + 1;
-        c.num0 = dg.o - k;
+        c.num0 = o - k;
         c.num1 = k + 1;
     } else {
         c.i0 = ci;
         c.i1 = -1;
-        c.num0 = dg.o + 1;
+        c.num0 = o + 1;
         c.num1 = 0;
     }
     return c;
+}
+
+__device__ __forceinline__ tdp_cover tdp_cover_1d(const tdp_dim_geom &dg, int32_t x)
+{
+    return tdp_cover_tab(dg.lo, dg.hi, dg.n, dg.L, dg.o, x);
 }
 
 // fp32 ramp weight num/(o+1), IEEE round-to-nearest division.

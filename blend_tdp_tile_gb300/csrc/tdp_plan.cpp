@@ -85,6 +85,8 @@ extern "C" tdp_status tdp_plan_create(const tdp_problem *prob, tdp_plan_t *out)
         return tdp_fail(TDP_ERR_UNSUPPORTED_DTYPE, "dtype must be TDP_F32 or TDP_BF16");
     if (prob->B < 0 || prob->C < 1 || prob->F < 1 || prob->H < 1 || prob->W < 1)
         return tdp_fail(TDP_ERR_INVALID_ARG, "need B >= 0 and C, F, H, W >= 1");
+    if (prob->F > (1 << 25) || prob->H > (1 << 25) || prob->W > (1 << 25))
+        return tdp_fail(TDP_ERR_TOO_LARGE, "F, H and W must be at most 2^25");
     const int32_t esize = prob->dtype == TDP_F32 ? 4 : 2;
     if (((int64_t)prob->C * esize) % 16 != 0)
         return tdp_fail(TDP_ERR_MISALIGNED, "C * element size must be a multiple of 16 bytes");

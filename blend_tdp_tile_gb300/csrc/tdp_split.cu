@@ -4,8 +4,9 @@
 //
 // Three launches on the caller's stream:
 //   1. tdp_bounds_init_kernel  mn = INT32_MAX, mx = INT32_MIN        (only with positions)
-//   2. tdp_bounds_kernel       per (tile, batch, tile-frame): min start / max end of the
-//                              tile's generated tokens, folded into mn/mx with atomics
+//   2. tdp_bounds_kernel       per (batch, frame, 8 rows; one warp per row): min start /
+//                              max end of every tile's generated tokens in those rows,
+//                              positions read once, folded into mn/mx with atomics
 //   3. tdp_split_kernel        scatter form: each latent row (b, f, h) is read ONCE with
 //                              16-byte loads and written to every tile row that holds it
 //                              (at most 2 x 2 x 2 tiles), positions likewise, shifted by
@@ -31,74 +32,83 @@ __global__ void tdp_bounds_init_kernel(int32_t *__restrict__ mn, int32_t *__rest
     }
 }
 
-// Block (t, b, fl): the tile-local frame fl of tile t, batch item b.  Reduces all
-// three dimensions over the frame's SH x SW tokens (every thread keeps
-// 3 * kBoundsUnroll loads in flight), then 6 atomics.
-constexpr int kBoundsUnroll = 4;
+// Block (b, f, chunk of kBoundsRows latent rows), one warp per row.  A warp
+// reads its row's positions once, 32 cells at a time (coalesced 256-byte
+// loads), and reduces each W-tile segment of the 32 cells with warp min / max
+// reductions (the tile loop is warp-uniform); lane 0 keeps the row's per-W-tile
+// minima / maxima in the warp's own shared-memory slots (no atomics).  The
+// block then combines its rows per (H-tile, W-tile, dim) and folds each result
+// into the (at most 2) F-tiles holding frame f with one atomicMin / atomicMax.
+constexpr int kBoundsRows = kBoundsThreads / 32;
 
 __global__ void __launch_bounds__(kBoundsThreads)
-tdp_bounds_kernel(const __grid_constant__ tdp_geom g, int32_t max_sf, const int2 *__restrict__ P,
+tdp_bounds_kernel(const __grid_constant__ tdp_geom g, const int2 *__restrict__ P,
                   int32_t *__restrict__ mn, int32_t *__restrict__ mx)
 {
-    const int32_t fl = blockIdx.x % max_sf;
-    const int32_t tb = blockIdx.x / max_sf;          // t*B + b
-    const int32_t t = tb / g.B, b = tb % g.B;
-    const int32_t nH = g.d[1].n, nW = g.d[2].n;
-    const int32_t iF = t / (nH * nW), iH = (t / nW) % nH, iW = t % nW;
-    const int32_t loF = g.d[0].lo[iF], SF = g.d[0].hi[iF] - loF;
-    if (fl >= SF) return;
-    const int32_t loH = g.d[1].lo[iH], SH = g.d[1].hi[iH] - loH;
-    const int32_t loW = g.d[2].lo[iW], SW = g.d[2].hi[iW] - loW;
-    const int64_t T = (int64_t)g.F * g.H * g.W;
-    const int32_t f = loF + fl;
-    const int2 *src0 = P + (int64_t)b * 3 * T + ((int64_t)f * g.H + loH) * g.W + loW;
-
-    int32_t lo[3] = {INT_MAX, INT_MAX, INT_MAX}, hi[3] = {INT_MIN, INT_MIN, INT_MIN};
-    const int32_t n = SH * SW;
-    for (int32_t e0 = threadIdx.x; e0 < n; e0 += kBoundsUnroll * blockDim.x) {
-        int2 v[kBoundsUnroll][3];
-#pragma unroll
-        for (int u = 0; u < kBoundsUnroll; ++u) {
-            const int32_t e = e0 + u * blockDim.x;
-            if (e < n) {
-                const int32_t hh = e / SW, ww = e - hh * SW;
-                const int64_t off = (int64_t)hh * g.W + ww;
-#pragma unroll
-                for (int d = 0; d < 3; ++d) v[u][d] = __ldg(src0 + d * T + off);
-            } else {
-#pragma unroll
-                for (int d = 0; d < 3; ++d) v[u][d] = make_int2(INT_MAX, INT_MIN);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kBoundsUnroll; ++u)
-#pragma unroll
-            for (int d = 0; d < 3; ++d) {
-                lo[d] = min(lo[d], v[u][d].x);
-                hi[d] = max(hi[d], v[u][d].y);
-            }
-    }
-    __shared__ int32_t s_mn[3][kBoundsThreads / 32], s_mx[3][kBoundsThreads / 32];
+    __shared__ int32_t s_mn[kBoundsRows][TDP_MAX_TILES_PER_DIM][3];
+    __shared__ int32_t s_mx[kBoundsRows][TDP_MAX_TILES_PER_DIM][3];
+    const int32_t nchunk = (g.H + kBoundsRows - 1) / kBoundsRows;
+    const int32_t chunk = blockIdx.x % nchunk;
+    const int32_t f = (blockIdx.x / nchunk) % g.F;
+    const int32_t b = blockIdx.x / (nchunk * g.F);
+    const int32_t h0 = chunk * kBoundsRows, h1 = min(g.H, h0 + kBoundsRows);
+    const int32_t nW = g.d[2].n, nH = g.d[1].n;
     const int32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int32_t h = h0 + warp;
+    const int64_t T = (int64_t)g.F * g.H * g.W;
+    const tdp_dim_geom &dW = g.d[2];
+
+    if (h < h1) {
+        for (int32_t i = lane; i < nW * 3; i += 32) {
+            (&s_mn[warp][0][0])[i] = INT_MAX;
+            (&s_mx[warp][0][0])[i] = INT_MIN;
+        }
+        __syncwarp();
+        const int2 *src = P + (int64_t)b * 3 * T + ((int64_t)f * g.H + h) * g.W;
+        int32_t iW = 0;
+        for (int32_t wb = 0; wb < g.W; wb += 32) {
+            const int32_t w = wb + lane;
+            int2 v[3];
 #pragma unroll
-    for (int d = 0; d < 3; ++d) {
-        const int32_t a = __reduce_min_sync(0xffffffffu, lo[d]);
-        const int32_t z = __reduce_max_sync(0xffffffffu, hi[d]);
-        if (lane == 0) {
-            s_mn[d][warp] = a;
-            s_mx[d][warp] = z;
+            for (int d = 0; d < 3; ++d) v[d] = w < g.W ? __ldg(src + (int64_t)d * T + w) : make_int2(INT_MAX, INT_MIN);
+            while (dW.hi[iW] <= wb) ++iW;                     // first W-tile touching [wb, wb + 32)
+            for (int32_t q = iW; q < nW && dW.lo[q] < wb + 32; ++q) {
+                const bool in = w >= dW.lo[q] && w < dW.hi[q] && w < g.W;
+#pragma unroll
+                for (int d = 0; d < 3; ++d) {
+                    const int32_t a = __reduce_min_sync(0xffffffffu, in ? v[d].x : INT_MAX);
+                    const int32_t z = __reduce_max_sync(0xffffffffu, in ? v[d].y : INT_MIN);
+                    if (lane == 0) {
+                        s_mn[warp][q][d] = min(s_mn[warp][q][d], a);
+                        s_mx[warp][q][d] = max(s_mx[warp][q][d], z);
+                    }
+                }
+            }
         }
     }
     __syncthreads();
-    if (threadIdx.x < 3) {
-        const int32_t d = threadIdx.x;
+    // combine the block's rows per (H-tile, W-tile, dim) and flush
+    const int32_t iHa = tdp_cover_1d(g.d[1], h0).i0;
+    const tdp_cover cHz = tdp_cover_1d(g.d[1], h1 - 1);
+    const int32_t iHb = cHz.i1 >= 0 ? cHz.i1 : cHz.i0;
+    const tdp_cover cF = tdp_cover_1d(g.d[0], f);
+    const int32_t nent = (iHb - iHa + 1) * nW * 3;
+    for (int32_t i = threadIdx.x; i < nent; i += blockDim.x) {
+        const int32_t iH = iHa + i / (nW * 3), iWq = (i / 3) % nW, d = i % 3;
+        const int32_t rlo = max(h0, g.d[1].lo[iH]), rhi = min(h1, g.d[1].hi[iH]);
         int32_t a = INT_MAX, z = INT_MIN;
-        for (int32_t w = 0; w < kBoundsThreads / 32; ++w) {
-            a = min(a, s_mn[d][w]);
-            z = max(z, s_mx[d][w]);
+        for (int32_t r = rlo; r < rhi; ++r) {
+            a = min(a, s_mn[r - h0][iWq][d]);
+            z = max(z, s_mx[r - h0][iWq][d]);
         }
-        atomicMin(mn + (int64_t)tb * 3 + d, a);
-        atomicMax(mx + (int64_t)tb * 3 + d, z);
+        if (rlo >= rhi || (a == INT_MAX && z == INT_MIN)) continue;   // nothing here (a no-op either way)
+        for (int q = 0; q < 2; ++q) {
+            const int32_t iF = q ? cF.i1 : cF.i0;
+            if (iF < 0) break;
+            const int64_t r = ((int64_t)((iF * nH + iH) * nW + iWq) * g.B + b) * 3 + d;
+            atomicMin(mn + r, a);
+            atomicMax(mx + r, z);
+        }
     }
 }
 
@@ -113,11 +123,18 @@ tdp_split_kernel(const __grid_constant__ tdp_geom g, const uint4 *__restrict__ X
     __shared__ int64_t s_Tt[TDP_MAX_COMBOS * TDP_MAX_TILES_PER_DIM];
     __shared__ int32_t s_tb[TDP_MAX_COMBOS * TDP_MAX_TILES_PER_DIM];
 
+    __shared__ int32_t s_loW[TDP_MAX_TILES_PER_DIM], s_hiW[TDP_MAX_TILES_PER_DIM];
+
     const int32_t row = blockIdx.x;
     const int32_t h = row % g.H, f = (row / g.H) % g.F, b = row / (g.H * g.F);
+    for (int32_t i = threadIdx.x; i < g.d[2].n; i += blockDim.x) {
+        s_loW[i] = g.d[2].lo[i];
+        s_hiW[i] = g.d[2].hi[i];
+    }
     const tdp_row_combos rc = tdp_make_combos(g, f, h);
     tdp_fill_row_table(g, rc, b, f, h, s_tok, P ? s_qpos : nullptr, P ? s_Tt : nullptr,
-                       P ? s_tb : nullptr);
+                       P ? s_tb : nullptr);   // ends with a barrier
+    const int32_t oW = g.d[2].o;
 
     const int32_t nW = g.d[2].n;
     const int32_t CV = (g.C * g.esize) >> 4;
@@ -130,7 +147,7 @@ tdp_split_kernel(const __grid_constant__ tdp_geom g, const uint4 *__restrict__ X
     for (int32_t v = threadIdx.x; v < nvec; v += blockDim.x) {
         const int32_t w = v / CV, cv = v - w * CV;
         const uint4 x = __ldcs(src + v);
-        const tdp_cover cW = tdp_cover_1d(g.d[2], w);
+        const tdp_cover cW = tdp_cover_tab(s_loW, s_hiW, nW, g.W, oW, w);
         for (int32_t c = 0; c < rc.nc; ++c) {
             __stcs(Y + (s_tok[c * nW + cW.i0] + w) * CV + cv, x);
             if (cW.i1 >= 0) __stcs(Y + (s_tok[c * nW + cW.i1] + w) * CV + cv, x);
@@ -142,7 +159,7 @@ tdp_split_kernel(const __grid_constant__ tdp_geom g, const uint4 *__restrict__ X
     for (int32_t q = threadIdx.x; q < 3 * g.W; q += blockDim.x) {
         const int32_t d = q / g.W, w = q - d * g.W;
         const int2 p = __ldcs(P + ((int64_t)b * 3 + d) * T + ((int64_t)f * g.H + h) * g.W + w);
-        const tdp_cover cW = tdp_cover_1d(g.d[2], w);
+        const tdp_cover cW = tdp_cover_tab(s_loW, s_hiW, nW, g.W, oW, w);
         for (int32_t c = 0; c < rc.nc; ++c) {
             for (int32_t k = 0; k < 2; ++k) {
                 const int32_t iW = k ? cW.i1 : cW.i0;
@@ -181,12 +198,9 @@ extern "C" tdp_status tdp_split(tdp_plan_t plan, const void *X, const int32_t *P
     if (pos) {
         const int32_t n = g.nt * g.B * 3;
         tdp_bounds_init_kernel<<<(n + 255) / 256, 256, 0, s>>>(mn, mx, n);
-        int32_t max_sf = 0;
-        for (int32_t i = 0; i < g.d[0].n; ++i) max_sf = max(max_sf, g.d[0].hi[i] - g.d[0].lo[i]);
-        const int64_t blocks = (int64_t)g.nt * g.B * max_sf;
-        if (blocks > 0x7fffffffLL) return tdp_fail(TDP_ERR_TOO_LARGE, "bounds grid too large");
-        tdp_bounds_kernel<<<(unsigned)blocks, kBoundsThreads, 0, s>>>(
-            g, max_sf, reinterpret_cast<const int2 *>(P), mn, mx);
+        const int64_t blocks = (int64_t)g.B * g.F * ((g.H + kBoundsRows - 1) / kBoundsRows);
+        tdp_bounds_kernel<<<(unsigned)blocks, kBoundsThreads, 0, s>>>(g, reinterpret_cast<const int2 *>(P), mn,
+                                                                       mx);
     }
     const int64_t rows = (int64_t)g.B * g.F * g.H;
     tdp_split_kernel<<<(unsigned)rows, kSplitThreads, 0, s>>>(

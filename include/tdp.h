@@ -97,9 +97,9 @@ typedef struct tdp_plan_s *tdp_plan_t;   /* opaque, host-owned */
  * [c_i - floor(o/2), c_{i+1} + (o - floor(o/2))), with no extension past 0
  * or L; neighbours overlap by exactly o cells.  Valid when 1 <= n <= L,
  * o >= 0 and, for n >= 2, floor(L/n) >= o (no cell lies in two overlaps);
- * for n = 1 the overlap is ignored.  Also checks B >= 0, C >= 1, the dtype,
- * C*esize % 16 == 0 and n <= TDP_MAX_TILES_PER_DIM, and that the 1-D masks of
- * every dimension sum exactly to one (integer check).
+ * for n = 1 the overlap is ignored.  Also checks B >= 0, C >= 1, F, H, W in
+ * [1, 2^25], the dtype, C*esize % 16 == 0 and n <= TDP_MAX_TILES_PER_DIM, and
+ * that the 1-D masks of every dimension sum exactly to one (integer check).
  *
  *   prob  host pointer, read only during the call.
  *   out   host pointer; receives a new plan on TDP_OK (unchanged otherwise).
