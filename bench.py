@@ -38,6 +38,7 @@ import workloads as wk  # noqa: E402
 METRIC = "TDP split+blend effective GB/s (fraction of GB300 HBM peak); latent tokens/s"
 WORKLOAD = "large"
 FALLBACK_HBM_GBS = 6800.0
+AUDIO_TOKENS = 2048          # synthetic per-tile audio latent for the tile-mean timing
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.txt")
 
 
@@ -301,6 +302,41 @@ def run_ours(args, rank, world, local_rank):
         "blend": statistics.mean(e[2].elapsed_time(e[3]) for e in per),
     }
 
+    # ---- the other reductions over tiles (outside the headline step): conditioning
+    # outputs averaged over the tiles that kept each token, audio mean over tiles
+    extras = None
+    if rank == 0 and not args.no_extras:
+        keep2, idx2, count2, kcount2, Kout2, slot2 = tdp.alloc_filter_outputs(plan, N, dev, slot=True)
+        tdp.tdp_norm_filter(plan, Kd, N, mn, mx, 1, keep2, idx2, count2, kcount2, Kout2, slot2, stream=s)
+        s.synchronize()
+        ncap = max(1, int(count2.max().item()))
+        kept_rows = int(count2.sum().item())
+        with torch.cuda.stream(s):
+            Yc = torch.randn((plan.n_tiles, wl.B, ncap, wl.C), generator=gen, device=dev).to(torch.bfloat16)
+            Oc = torch.empty((wl.B, N, wl.C), dtype=torch.bfloat16, device=dev)
+            La = AUDIO_TOKENS * wl.C
+            Au = torch.randn((plan.n_tiles, wl.B, La), generator=gen, device=dev).to(torch.bfloat16)
+            Ou = torch.empty((wl.B, La), dtype=torch.bfloat16, device=dev)
+        s.synchronize()
+        extras = {}
+        for name, fn, nbytes in (
+            ("cond_blend", lambda: tdp.tdp_cond_blend(plan, N, ncap, Yc, slot2, Oc, stream=s),
+             kept_rows * wl.C * wl.esize + plan.n_tiles * wl.B * N * 4 + wl.B * N * wl.C * wl.esize),
+            ("tile_mean", lambda: tdp.tdp_tile_mean(plan, La, Au, Ou, stream=s),
+             (plan.n_tiles + 1) * wl.B * La * wl.esize)):
+            for _ in range(5):
+                fn()
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(s)
+            for _ in range(100):
+                fn()
+            a1.record(s)
+            s.synchronize()
+            t_ms = a0.elapsed_time(a1) / 100
+            extras[name] = {"ms": t_ms, "algorithmic_bytes": nbytes, "GB/s": nbytes / (t_ms * 1e-3) / 1e9}
+        extras["cond_blend"]["shape"] = f"{plan.n_tiles} tiles x {ncap} rows x {wl.C} ch, {kept_rows} kept rows"
+        extras["tile_mean"]["shape"] = f"{plan.n_tiles} tiles x {AUDIO_TOKENS} audio tokens x {wl.C} ch (synthetic)"
+
     # ---- end to end, through the C ABI: every step copies its inputs (latent,
     # positions, cond tokens) from pinned host memory and reads its blended latent
     # back.  Three streams: step i+1's host->device copies and step i-1's
@@ -395,6 +431,7 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": 5 * args.steps,
         "clocks": sampler.summary(t0, t1) if sampler else None,
         "e2e": e2e,
+        "extra_kernels": extras,
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, X, P, K)
@@ -448,6 +485,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip the timing of the extra reductions")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -26,7 +26,8 @@ import numpy as np
 __all__ = [
     "TDP_OK", "TDP_F32", "TDP_BF16", "TDP_MAX_TILES_PER_DIM", "TdpError",
     "Plan", "tdp_plan_create", "tdp_plan_info", "tdp_plan_destroy",
-    "tdp_split", "tdp_norm_filter", "tdp_blend", "tdp_status_str", "tdp_last_error_detail",
+    "tdp_split", "tdp_norm_filter", "tdp_blend", "tdp_cond_blend", "tdp_tile_mean",
+    "tdp_status_str", "tdp_last_error_detail",
     "alloc_split_outputs", "alloc_filter_outputs", "LIB_PATH",
 ]
 
@@ -66,8 +67,12 @@ def _load():
     lib.tdp_plan_destroy.restype = None
     lib.tdp_split.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp]
     lib.tdp_split.restype = ctypes.c_int
-    lib.tdp_norm_filter.argtypes = [vp, vp, i32, vp, vp, i32, vp, vp, vp, vp, vp, vp]
+    lib.tdp_norm_filter.argtypes = [vp, vp, i32, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp]
     lib.tdp_norm_filter.restype = ctypes.c_int
+    lib.tdp_cond_blend.argtypes = [vp, i32, i32, vp, vp, vp, vp]
+    lib.tdp_cond_blend.restype = ctypes.c_int
+    lib.tdp_tile_mean.argtypes = [vp, ctypes.c_int64, vp, vp, vp]
+    lib.tdp_tile_mean.restype = ctypes.c_int
     lib.tdp_blend.argtypes = [vp, vp, vp, vp]
     lib.tdp_blend.restype = ctypes.c_int
     lib.tdp_status_str.argtypes = [ctypes.c_int]
@@ -213,8 +218,10 @@ def tdp_split(plan: Plan, X, P, normalize, Y, Q, mn, mx, stream=None):
     _check(_lib.tdp_split(plan.handle, *args), "tdp_split")
 
 
-def tdp_norm_filter(plan: Plan, K, N, mn, mx, normalize, keep, idx, count, kcount, Kout, stream=None):
-    """Per-tile keep / compaction / normalisation of conditioning tokens K [B,3,N,2]."""
+def tdp_norm_filter(plan: Plan, K, N, mn, mx, normalize, keep, idx, count, kcount, Kout, slot=None,
+                    stream=None):
+    """Per-tile keep / compaction / normalisation of conditioning tokens K [B,3,N,2]
+    (and, if `slot` is given, each token's position in every tile's kept list)."""
     torch = _torch()
     B, nt = plan.B, plan.n_tiles
     N = int(N)
@@ -229,9 +236,30 @@ def tdp_norm_filter(plan: Plan, K, N, mn, mx, normalize, keep, idx, count, kcoun
         _ptr(count, "count", nt * B, i32, 4),
         _ptr(kcount, "kcount", B * N, i32, 4),
         _ptr(Kout, "Kout", nt * B * 3 * N * 2, i32, 8),
+        _ptr(slot, "slot", nt * B * N, i32, 4),
         _stream(stream),
     )
     _check(_lib.tdp_norm_filter(plan.handle, *args), "tdp_norm_filter")
+
+
+def tdp_cond_blend(plan: Plan, N, ncap, Ycond, slot, out, stream=None):
+    """Average each conditioning token's per-tile outputs Ycond [nt,B,ncap,C] over the tiles
+    that kept it (slot from tdp_norm_filter) into out [B,N,C]."""
+    torch = _torch()
+    B, nt, C = plan.B, plan.n_tiles, plan.C
+    N, ncap = int(N), int(ncap)
+    lat = _latent_dtypes(plan)
+    _check(_lib.tdp_cond_blend(plan.handle, N, ncap, _ptr(Ycond, "Ycond", nt * B * ncap * C, lat, 16),
+                               _ptr(slot, "slot", nt * B * N, (torch.int32,), 4),
+                               _ptr(out, "out", B * N * C, lat, 16), _stream(stream)), "tdp_cond_blend")
+
+
+def tdp_tile_mean(plan: Plan, L, A, out, stream=None):
+    """Mean over tiles of A [nt,B,L] into out [B,L] (the audio path)."""
+    B, nt, L = plan.B, plan.n_tiles, int(L)
+    lat = _latent_dtypes(plan)
+    _check(_lib.tdp_tile_mean(plan.handle, L, _ptr(A, "A", nt * B * L, lat, 16),
+                              _ptr(out, "out", B * L, lat, 16), _stream(stream)), "tdp_tile_mean")
 
 
 def tdp_blend(plan: Plan, Yout, Z, stream=None):
@@ -256,8 +284,8 @@ def alloc_split_outputs(plan: Plan, device="cuda", positions=True):
     return Y, Q, mn, mx
 
 
-def alloc_filter_outputs(plan: Plan, N: int, device="cuda"):
-    """keep, idx [nt,B,N], count [nt,B], kcount [B,N], Kout [nt,B,3,N,2]."""
+def alloc_filter_outputs(plan: Plan, N: int, device="cuda", slot=False):
+    """keep, idx [nt,B,N], count [nt,B], kcount [B,N], Kout [nt,B,3,N,2] (and slot [nt,B,N])."""
     torch = _torch()
     nt, B = plan.n_tiles, plan.B
     keep = torch.empty((nt, B, N), dtype=torch.uint8, device=device)
@@ -265,4 +293,6 @@ def alloc_filter_outputs(plan: Plan, N: int, device="cuda"):
     count = torch.empty((nt, B), dtype=torch.int32, device=device)
     kcount = torch.empty((B, N), dtype=torch.int32, device=device)
     Kout = torch.empty((nt, B, 3, N, 2), dtype=torch.int32, device=device)
+    if slot:
+        return keep, idx, count, kcount, Kout, torch.empty((nt, B, N), dtype=torch.int32, device=device)
     return keep, idx, count, kcount, Kout

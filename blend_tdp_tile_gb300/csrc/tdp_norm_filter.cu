@@ -8,7 +8,8 @@
 //      keeps the 16 ballots; the 16 x 32 table of per-(j, warp) counts is
 //      scanned once in (j, warp) order, so token k's slot is its table offset
 //      plus its rank within its ballot: ascending order, no atomics.  Kept
-//      tokens are written shifted by mn.
+//      tokens are written shifted by mn, and (optionally) every token's slot in
+//      the kept list (or -1).
 //   2. keep counts: the B*n_tiles blocks split each batch item's tokens into
 //      n_tiles slices; a block counts, for each token of its slice, the tiles
 //      that keep it (the 1/(tiles that kept it) weight's denominator) by
@@ -43,7 +44,7 @@ __global__ void __launch_bounds__(kFilterThreads, 1)
 tdp_filter_kernel(const __grid_constant__ tdp_geom g, const int2 *__restrict__ K, int32_t N,
                   const int32_t *__restrict__ mn, const int32_t *__restrict__ mx, int32_t normalize,
                   uint8_t *__restrict__ keep, int32_t *__restrict__ idx, int32_t *__restrict__ count,
-                  int32_t *__restrict__ kcount, int2 *__restrict__ Kout)
+                  int32_t *__restrict__ kcount, int2 *__restrict__ Kout, int32_t *__restrict__ slot)
 {
     __shared__ int32_t s_off[kSub][kWarps];       // per (sub-chunk, warp): kept count, then offset
     __shared__ int32_t s_total;
@@ -113,8 +114,12 @@ tdp_filter_kernel(const __grid_constant__ tdp_geom g, const int2 *__restrict__ K
         __syncthreads();
 #pragma unroll
         for (int j = 0; j < kSub; ++j) {
-            if ((ballots[j] >> lane) & 1u) {
-                const int32_t k = k0 + j * kFilterThreads + warp * 32 + lane;
+            const int32_t kj = k0 + j * kFilterThreads + warp * 32 + lane;
+            const bool kept = (ballots[j] >> lane) & 1u;
+            if (slot && kj < N)
+                slot[(int64_t)tb * N + kj] = kept ? base + s_off[j][warp] + __popc(ballots[j] & lt_mask) : -1;
+            if (kept) {
+                const int32_t k = kj;
                 const int32_t pos = base + s_off[j][warp] + __popc(ballots[j] & lt_mask);
                 idx[(int64_t)tb * N + pos] = k;
 #pragma unroll
@@ -179,7 +184,7 @@ tdp_filter_kernel(const __grid_constant__ tdp_geom g, const int2 *__restrict__ K
 extern "C" tdp_status tdp_norm_filter(tdp_plan_t plan, const int32_t *K, int32_t N,
                                       const int32_t *mn, const int32_t *mx, int32_t normalize,
                                       uint8_t *keep, int32_t *idx, int32_t *count, int32_t *kcount,
-                                      int32_t *Kout, tdp_stream_t stream)
+                                      int32_t *Kout, int32_t *slot, tdp_stream_t stream)
 {
     if (!plan) return tdp_fail(TDP_ERR_INVALID_ARG, "null plan");
     const tdp_geom &g = plan->g;
@@ -190,7 +195,7 @@ extern "C" tdp_status tdp_norm_filter(tdp_plan_t plan, const int32_t *K, int32_t
         return tdp_fail(TDP_ERR_INVALID_ARG, "null K, keep, idx, kcount or Kout");
     if (!tdp_aligned(mn, 4) || !tdp_aligned(mx, 4) || !tdp_aligned(count, 4) ||
         (N > 0 && (!tdp_aligned(K, 8) || !tdp_aligned(Kout, 8) || !tdp_aligned(idx, 4) ||
-                   !tdp_aligned(kcount, 4))))
+                   !tdp_aligned(kcount, 4) || !tdp_aligned(slot, 4))))
         return tdp_fail(TDP_ERR_MISALIGNED, "K, Kout need 8-byte and int32 buffers 4-byte alignment");
     const int64_t blocks = (int64_t)g.nt * g.B;    // one block per (tile, batch item)
     if (blocks > 0x7fffffffLL || (int64_t)g.B * N * g.nt > ((int64_t)1 << 56))
@@ -198,7 +203,7 @@ extern "C" tdp_status tdp_norm_filter(tdp_plan_t plan, const int32_t *K, int32_t
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     tdp_filter_kernel<<<(unsigned)blocks, kFilterThreads, 0, s>>>(
         g, reinterpret_cast<const int2 *>(K), N, mn, mx, normalize, keep, idx, count, kcount,
-        reinterpret_cast<int2 *>(Kout));
+        reinterpret_cast<int2 *>(Kout), slot);
     const cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return tdp_fail(TDP_ERR_CUDA, cudaGetErrorString(err));
     return tdp_ok();

@@ -167,12 +167,53 @@ tdp_status tdp_split(tdp_plan_t plan, const void *X, const int32_t *P, int32_t n
  *              (the denominator of the page's 1/(tiles that kept it) weight).
  *   Kout       device [n_tiles,B,3,N,2] int32: entries [t,b,d,0:count) are the
  *              kept tokens' intervals in idx order; entries past count are not written.
+ *   slot       device [n_tiles,B,N] int32, or NULL: token k's position in (t,b)'s
+ *              kept list, or -1 (the inverse of idx; input of tdp_cond_blend).
  *   stream     CUDA stream.
  */
 tdp_status tdp_norm_filter(tdp_plan_t plan, const int32_t *K, int32_t N,
                            const int32_t *mn, const int32_t *mx, int32_t normalize,
                            uint8_t *keep, int32_t *idx, int32_t *count, int32_t *kcount,
-                           int32_t *Kout, tdp_stream_t stream);
+                           int32_t *Kout, int32_t *slot, tdp_stream_t stream);
+
+/*
+ * tdp_cond_blend -- average each conditioning token's per-tile outputs over the
+ * tiles that kept it.
+ * ("Shared negative (reference) positions": a token kept by several tiles has
+ *  blend weight 1/(number of tiles that kept it), so that it is not counted
+ *  several times.)
+ *
+ * out[b,k,:] = (1/n) * sum over the tiles t that kept token k, ascending, of
+ * Ycond[t,b,slot[t,b,k],:], n = number of those tiles; fp32 accumulation, one
+ * division per element by n, stored in the plan's dtype.  A token that no tile
+ * kept gets 0.
+ *
+ *   N      conditioning tokens per batch item (>= 0).
+ *   ncap   rows reserved per (tile, batch item) in Ycond (>= 1); slots >= ncap
+ *          are ignored, so ncap >= max count keeps every contribution.
+ *   Ycond  device [n_tiles, B, ncap, C] (plan dtype): row p of (t,b) is the
+ *          per-tile transformer's output for the p-th token t kept for item b.
+ *   slot   device [n_tiles, B, N] int32 from tdp_norm_filter.
+ *   out    device [B, N, C] (plan dtype), written.
+ *   stream CUDA stream.
+ */
+tdp_status tdp_cond_blend(tdp_plan_t plan, int32_t N, int32_t ncap, const void *Ycond,
+                          const int32_t *slot, void *out, tdp_stream_t stream);
+
+/*
+ * tdp_tile_mean -- mean over tiles of a per-tile untiled output (the audio path).
+ * ("What it is": audio is processed untiled on every tile's forward pass and
+ *  averaged across tiles; the page warns that this average is context for the
+ *  video tiles, not a meaningful audio output.)
+ *
+ * out[b,l] = (sum over t of A[t,b,l]) / n_tiles, fp32 accumulation in ascending
+ * t, stored in the plan's dtype.
+ *
+ *   L    elements per batch item; L * sizeof(element) must be a multiple of 16.
+ *   A    device [n_tiles, B, L] (plan dtype), read.
+ *   out  device [B, L] (plan dtype), written.
+ */
+tdp_status tdp_tile_mean(tdp_plan_t plan, int64_t L, const void *A, void *out, tdp_stream_t stream);
 
 /*
  * tdp_blend -- mask-weighted accumulation of all tile outputs into the latent.

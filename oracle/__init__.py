@@ -16,7 +16,9 @@ from this code): the tiny workload's 3x5x7 tile size, exact integer partition
 of unity of the ramps, linear ramps, split == numpy box slicing, identity for
 one tile, pure permutation for zero overlap, blend(split(X)) == X, closed-form
 offsets for grid positions, negative-time tokens kept by every tile, cell
-enumeration for the keep rule, and an exact-rational brute force of the blend.
+enumeration for the keep rule, an exact-rational brute force of the blend,
+and, for the conditioning-output average and the audio tile mean, identity
+outputs, per-tile constants, single-keeper tokens and one-tile copies.
 """
 from __future__ import annotations
 
@@ -75,12 +77,16 @@ def _load():
             lib.oracle_bounds.restype = None
             lib.oracle_normalize.argtypes = [P, vp, vp]
             lib.oracle_normalize.restype = None
-            lib.oracle_filter.argtypes = [P, vp, i32, vp, vp, i32, vp, vp, vp, vp, vp]
+            lib.oracle_filter.argtypes = [P, vp, i32, vp, vp, i32, vp, vp, vp, vp, vp, vp]
             lib.oracle_filter.restype = None
             lib.oracle_blend.argtypes = [P, vp, vp]
             lib.oracle_blend.restype = None
             lib.oracle_blend_cell.argtypes = [P, vp, i32, i32, i32, i32, vp]
             lib.oracle_blend_cell.restype = None
+            lib.oracle_cond_blend.argtypes = [P, i32, i32, vp, vp, vp, vp, vp]
+            lib.oracle_cond_blend.restype = None
+            lib.oracle_tile_mean.argtypes = [P, vp, ctypes.c_int64, vp]
+            lib.oracle_tile_mean.restype = None
             _lib = lib
     return _lib
 
@@ -166,8 +172,9 @@ def normalize(p: Problem, Q: np.ndarray, mn: np.ndarray) -> np.ndarray:
     return Qn
 
 
-def filter_cond(p: Problem, K: np.ndarray, mn, mx, normalize_positions: bool = True):
-    """(keep[nt,B,N] u8, idx[nt,B,N], count[nt,B], kcount[B,N], Kout[nt,B,3,N,2])."""
+def filter_cond(p: Problem, K: np.ndarray, mn, mx, normalize_positions: bool = True, with_slot: bool = False):
+    """(keep[nt,B,N] u8, idx[nt,B,N], count[nt,B], kcount[B,N], Kout[nt,B,3,N,2]) and, with
+    `with_slot`, slot[nt,B,N] (token k's position in (t,b)'s kept list, or -1)."""
     nt = p.n[0] * p.n[1] * p.n[2]
     K = np.ascontiguousarray(K, dtype=np.int32)
     N = K.shape[2]
@@ -176,11 +183,34 @@ def filter_cond(p: Problem, K: np.ndarray, mn, mx, normalize_positions: bool = T
     count = np.zeros((nt, p.B), np.int32)
     kcount = np.zeros((p.B, N), np.int32)
     Kout = np.zeros((nt, p.B, 3, N, 2), np.int32)
+    slot = np.zeros((nt, p.B, N), np.int32)
     _load().oracle_filter(ctypes.byref(p), _ptr(K), N,
                           _ptr(np.ascontiguousarray(mn, np.int32)), _ptr(np.ascontiguousarray(mx, np.int32)),
                           int(bool(normalize_positions)),
-                          _ptr(keep), _ptr(idx), _ptr(count), _ptr(kcount), _ptr(Kout))
+                          _ptr(keep), _ptr(idx), _ptr(count), _ptr(kcount), _ptr(Kout), _ptr(slot))
+    if with_slot:
+        return keep, idx, count, kcount, Kout, slot
     return keep, idx, count, kcount, Kout
+
+
+def cond_blend(p: Problem, Ycond: np.ndarray, keep, idx, count, ncap: int) -> np.ndarray:
+    """out[B,N,C] float64: each conditioning token's outputs averaged over the tiles that kept it."""
+    N = keep.shape[2]
+    Ycond = np.ascontiguousarray(Ycond, dtype=_elem_dtype(p))
+    out = np.zeros((p.B, N, p.C), np.float64)
+    _load().oracle_cond_blend(ctypes.byref(p), N, ncap, _ptr(Ycond),
+                              _ptr(np.ascontiguousarray(keep, np.uint8)),
+                              _ptr(np.ascontiguousarray(idx, np.int32)),
+                              _ptr(np.ascontiguousarray(count, np.int32)), _ptr(out))
+    return out
+
+
+def tile_mean(p: Problem, A: np.ndarray, L: int) -> np.ndarray:
+    """out[B,L] float64: mean over tiles of A[nt,B,L]."""
+    A = np.ascontiguousarray(A, dtype=_elem_dtype(p))
+    out = np.zeros((p.B, L), np.float64)
+    _load().oracle_tile_mean(ctypes.byref(p), _ptr(A), L, _ptr(out))
+    return out
 
 
 def blend(p: Problem, Yout: np.ndarray) -> np.ndarray:

@@ -247,11 +247,13 @@ void oracle_normalize(const oracle_problem *p, int32_t *Q, const int32_t *mn)
  * "negative time" is start_F < 0; the test uses global (un-normalised)
  * coordinates; keep is decided per batch item; kept tokens are listed in
  * ascending k.  idx is padded with -1 past count; Kout past count is not
- * written.  kcount[b,k] is the number of tiles that kept token k.
+ * written.  kcount[b,k] is the number of tiles that kept token k; slot[t,b,k]
+ * is token k's position in (t,b)'s kept list, or -1.
  * ---------------------------------------------------------------------- */
 void oracle_filter(const oracle_problem *p, const int32_t *K, int32_t N,
                    const int32_t *mn, const int32_t *mx, int32_t normalize,
-                   uint8_t *keep, int32_t *idx, int32_t *count, int32_t *kcount, int32_t *Kout)
+                   uint8_t *keep, int32_t *idx, int32_t *count, int32_t *kcount, int32_t *Kout,
+                   int32_t *slot)
 {
     int nt = oracle_num_tiles(p);
     for (int64_t i = 0; i < (int64_t)p->B * N; ++i) kcount[i] = 0;
@@ -271,6 +273,7 @@ void oracle_filter(const oracle_problem *p, const int32_t *K, int32_t N,
                 int negative_time = K[(((int64_t)b * 3 + 0) * N + k) * 2 + 0] < 0;
                 int kept = inside || negative_time;
                 keep[tb * N + k] = (uint8_t)kept;
+                slot[tb * N + k] = kept ? cnt : -1;
                 if (kept) {
                     idx[tb * N + cnt] = k;
                     for (int d = 0; d < 3; ++d)
@@ -351,4 +354,53 @@ void oracle_blend_cell(const oracle_problem *p, const void *Yout, int32_t b,
     }
     free(box);
     free(off);
+}
+
+/* ------------------------------------------------------------------------
+ * Conditioning-token output reduction ("Shared negative (reference)
+ * positions": a token kept by several tiles has blend weight
+ * 1 / (number of tiles that kept it)).  Ycond holds each tile's outputs for its
+ * kept conditioning tokens, [nt][B][ncap][C], row p of (t,b) = the p-th kept
+ * token.  out[b,k,:] = sum over the tiles t that kept k (ascending) of
+ * Ycond[t,b,slot,:] / kcount[b,k], in fp64.
+ * Reading taken: a token no tile kept has no tile output; its result is 0.
+ * ---------------------------------------------------------------------- */
+void oracle_cond_blend(const oracle_problem *p, int32_t N, int32_t ncap, const void *Ycond,
+                       const uint8_t *keep, const int32_t *idx, const int32_t *count, double *out)
+{
+    int nt = oracle_num_tiles(p);
+    for (int32_t b = 0; b < p->B; ++b)
+        for (int32_t k = 0; k < N; ++k) {
+            double *o = out + ((int64_t)b * N + k) * p->C;
+            for (int32_t c = 0; c < p->C; ++c) o[c] = 0.0;
+            int32_t kept_by = 0;
+            for (int t = 0; t < nt; ++t) {
+                int64_t tb = (int64_t)t * p->B + b;
+                if (!keep[tb * N + k]) continue;
+                int32_t pos = -1;                    /* find k in the tile's kept list */
+                for (int32_t q = 0; q < count[tb]; ++q)
+                    if (idx[tb * N + q] == k) { pos = q; break; }
+                if (pos < 0 || pos >= ncap) continue;
+                kept_by += 1;
+                for (int32_t c = 0; c < p->C; ++c)
+                    o[c] += load_elem(Ycond, p->esize, (tb * ncap + pos) * p->C + c);
+            }
+            if (kept_by > 0)
+                for (int32_t c = 0; c < p->C; ++c) o[c] /= (double)kept_by;
+        }
+}
+
+/* ------------------------------------------------------------------------
+ * Audio mean ("What it is": audio is processed untiled on every tile's forward
+ * pass and averaged across tiles).  A is [nt][B][L] (L elements of one audio
+ * latent per batch item); out[b,l] = (1/nt) * sum over t of A[t,b,l], fp64.
+ * ---------------------------------------------------------------------- */
+void oracle_tile_mean(const oracle_problem *p, const void *A, int64_t L, double *out)
+{
+    int nt = oracle_num_tiles(p);
+    for (int64_t i = 0; i < (int64_t)p->B * L; ++i) {
+        double acc = 0.0;
+        for (int t = 0; t < nt; ++t) acc += load_elem(A, p->esize, (int64_t)t * p->B * L + i);
+        out[i] = acc / (double)nt;
+    }
 }

@@ -52,13 +52,13 @@ def run_split_filter(tdp, plan, wl, X, P, K, normalize=True, stream=None, positi
     if positions:
         out.update(Q=to_host(Q), mn=to_host(mn), mx=to_host(mx))
         N = K.shape[2]
-        keep, idx, count, kcount, Kout = tdp.alloc_filter_outputs(plan, N, dev)
-        for t in (keep, idx, count, kcount, Kout):
+        keep, idx, count, kcount, Kout, slot = tdp.alloc_filter_outputs(plan, N, dev, slot=True)
+        for t in (keep, idx, count, kcount, Kout, slot):
             fill_sentinel(t)
         tdp.tdp_norm_filter(plan, to_dev(K), N, mn, mx, normalize, keep, idx, count, kcount, Kout,
-                            stream=stream)
+                            slot, stream=stream)
         out.update(keep=to_host(keep), idx=to_host(idx), count=to_host(count),
-                   kcount=to_host(kcount), Kout=to_host(Kout))
+                   kcount=to_host(kcount), Kout=to_host(Kout), slot=to_host(slot), slotd=slot)
     if stream is not None:
         stream.synchronize()
     torch.cuda.synchronize()
@@ -104,6 +104,8 @@ def assert_blend_close(z: np.ndarray, ref: np.ndarray, wl):
 
 def assert_filter_equal(out, ref, nt, B):
     assert np.array_equal(out["keep"], ref["keep"])
+    if "slot" in ref and "slot" in out:
+        assert np.array_equal(out["slot"], ref["slot"])
     assert np.array_equal(out["idx"], ref["idx"])
     assert np.array_equal(out["count"], ref["count"])
     assert np.array_equal(out["kcount"], ref["kcount"])

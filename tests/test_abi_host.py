@@ -132,15 +132,24 @@ def test_host_validation_before_launch(tdp):
     vp = ctypes.c_void_p
     lib.tdp_split.argtypes = [vp, vp, vp, ctypes.c_int32, vp, vp, vp, vp, vp]
     lib.tdp_blend.argtypes = [vp, vp, vp, vp]
-    lib.tdp_norm_filter.argtypes = [vp, vp, ctypes.c_int32, vp, vp, ctypes.c_int32, vp, vp, vp, vp, vp, vp]
+    lib.tdp_norm_filter.argtypes = [vp, vp, ctypes.c_int32, vp, vp, ctypes.c_int32, vp, vp, vp, vp, vp, vp, vp]
+    lib.tdp_cond_blend.argtypes = [vp, ctypes.c_int32, ctypes.c_int32, vp, vp, vp, vp]
+    lib.tdp_tile_mean.argtypes = [vp, ctypes.c_int64, vp, vp, vp]
     # positions half given
     assert lib.tdp_split(plan.handle, 16, 8, 1, 16, None, None, None, None) == 1
     # misaligned latent pointer (never dereferenced: refused on the host)
     assert lib.tdp_split(plan.handle, 24, None, 1, 16, None, None, None, None) == 4
     assert lib.tdp_blend(plan.handle, 16, 40, None) == 4
     assert lib.tdp_blend(plan.handle, None, 16, None) == 1
-    assert lib.tdp_norm_filter(plan.handle, None, -1, 16, 16, 1, None, None, 16, None, None, None) == 1
-    assert lib.tdp_norm_filter(plan.handle, 8, 4, 16, 16, 1, 16, 16, 16, 16, 12, None) == 4
+    assert lib.tdp_norm_filter(plan.handle, None, -1, 16, 16, 1, None, None, 16, None, None, None, None) == 1
+    assert lib.tdp_norm_filter(plan.handle, 8, 4, 16, 16, 1, 16, 16, 16, 16, 12, None, None) == 4
+    assert lib.tdp_norm_filter(plan.handle, 8, 4, 16, 16, 1, 16, 16, 16, 16, 16, 6, None) == 4   # slot
+    assert lib.tdp_cond_blend(plan.handle, 4, 0, 16, 16, 16, None) == 1                           # ncap < 1
+    assert lib.tdp_cond_blend(plan.handle, 4, 4, 24, 16, 16, None) == 4                           # Ycond
+    assert lib.tdp_cond_blend(plan.handle, 4, 4, 16, None, 16, None) == 1
+    assert lib.tdp_tile_mean(plan.handle, 3, 16, 16, None) == 4                                   # 12 bytes
+    assert lib.tdp_tile_mean(plan.handle, 8, 16, 40, None) == 4
+    assert lib.tdp_tile_mean(plan.handle, -1, 16, 16, None) == 1
 
 
 def test_binding_refuses_wrong_sizes_on_host(tdp):

@@ -47,7 +47,8 @@ def _check_path(tdp, wl, X, P, K, normalize=True, stream=None):
     assert np.array_equal(out["mn"], mn) and np.array_equal(out["mx"], mx)
     Qn = oracle.normalize(p, Qref, mn) if normalize else Qref
     assert np.array_equal(out["Q"], Qn), "tile positions differ"
-    ref = dict(zip(("keep", "idx", "count", "kcount", "Kout"), oracle.filter_cond(p, K, mn, mx, normalize)))
+    ref = dict(zip(("keep", "idx", "count", "kcount", "Kout", "slot"),
+                   oracle.filter_cond(p, K, mn, mx, normalize, with_slot=True)))
     assert_filter_equal(out, ref, plan.n_tiles, wl.B)
     # blend of noisy tile outputs
     Yout = _yout(wl, Yref, wl.seed + 99)
@@ -189,7 +190,8 @@ def test_large_workload_in_bench_configuration(tdp):
     assert np.array_equal(out["mn"], mn) and np.array_equal(out["mx"], mx)
     assert np.array_equal(out["Q"], oracle.normalize(p, Qref, mn))
     del Qref
-    ref = dict(zip(("keep", "idx", "count", "kcount", "Kout"), oracle.filter_cond(p, K, mn, mx, True)))
+    ref = dict(zip(("keep", "idx", "count", "kcount", "Kout", "slot"),
+                   oracle.filter_cond(p, K, mn, mx, True, with_slot=True)))
     assert_filter_equal(out, ref, plan.n_tiles, wl.B)
     # reconstruction over the whole latent
     Zr = run_blend(tdp, plan, wl, out["Yd"])

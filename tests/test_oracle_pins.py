@@ -438,3 +438,93 @@ def test_oracle_is_independent_of_cuda_path():
             assert "import blend_tdp_tile_gb300" not in src
             assert "from blend_tdp_tile_gb300" not in src
             assert "#include \"tdp.h\"" not in src and "libtdp" not in src
+
+
+# --------------------------------------------------------------------------- conditioning outputs / audio
+def _filtered(wl, n_cond=None, seed=21):
+    p = oracle.problem_of(wl)
+    X, P, _ = wk.make_inputs(wl)
+    K = wk.make_cond_positions(wl, np.random.default_rng(seed), n_cond=n_cond)
+    _, Q = oracle.split(p, X, P)
+    mn, mx = oracle.bounds(p, Q)
+    keep, idx, count, kcount, Kout, slot = oracle.filter_cond(p, K, mn, mx, True, with_slot=True)
+    return p, K, keep, idx, count, kcount, slot
+
+
+def test_slot_is_inverse_of_compaction():
+    wl = wk.by_name("small")
+    p, K, keep, idx, count, kcount, slot = _filtered(wl, n_cond=300)
+    for t in range(keep.shape[0]):
+        for b in range(wl.B):
+            c = count[t, b]
+            assert np.array_equal(slot[t, b, idx[t, b, :c]], np.arange(c))
+            assert (slot[t, b][keep[t, b] == 0] == -1).all()
+
+
+@pytest.mark.parametrize("name", ["tiny", "small", "temporal"])
+def test_cond_blend_identity_outputs_give_back_features(name):
+    """If every tile returns each kept token's own feature, the average over the keeping
+    tiles is that feature; a token no tile kept gets 0."""
+    wl = wk.by_name(name).replace(n_cond=min(wk.by_name(name).n_cond, 600))
+    p, K, keep, idx, count, kcount, slot = _filtered(wl)
+    nt, N = keep.shape[0], keep.shape[2]
+    feat = (np.random.default_rng(2).integers(-64, 64, size=(wl.B, N, wl.C)) / 16).astype(np.float32)
+    Yc = np.zeros((nt, wl.B, N, wl.C), np.float32)
+    for t in range(nt):
+        for b in range(wl.B):
+            c = count[t, b]
+            Yc[t, b, :c] = feat[b, idx[t, b, :c]]
+    if wl.dtype == "bf16":
+        Yc = wk.f32_to_bf16_bits(Yc)       # features are exact in bf16 (multiples of 1/16, |x| <= 4)
+    out = oracle.cond_blend(p, Yc, keep, idx, count, N)
+    kept = kcount > 0
+    assert np.allclose(out[kept], feat[kept], rtol=0, atol=1e-12)
+    assert (out[~kept] == 0).all()
+
+
+def test_cond_blend_constant_per_tile_outputs():
+    """Tile t returning the constant t for every token: the result is the mean tile index
+    over the keeping tiles, and (n_tiles-1)/2 for negative-time tokens."""
+    wl = wk.by_name("temporal").replace(n_cond=500)
+    p, K, keep, idx, count, kcount, slot = _filtered(wl)
+    nt, N = keep.shape[0], keep.shape[2]
+    Yc = np.broadcast_to(np.arange(nt, dtype=np.float32)[:, None, None, None], (nt, wl.B, N, wl.C)).copy()
+    out = oracle.cond_blend(p, wk.f32_to_bf16_bits(Yc), keep, idx, count, N)
+    tiles = np.arange(nt, dtype=np.float64)[:, None, None]
+    with np.errstate(invalid="ignore", divide="ignore"):
+        expect = (keep * tiles).sum(axis=0) / kcount
+    kept = kcount > 0
+    assert np.allclose(out[..., 0][kept], expect[kept], rtol=0, atol=1e-12)
+    neg = K[:, 0, :, 0] < 0
+    assert np.allclose(out[..., 0][neg], (nt - 1) / 2, atol=1e-12)
+
+
+def test_cond_blend_single_keeper_is_exact_and_linear():
+    wl = wk.by_name("small").replace(n_cond=400)
+    p, K, keep, idx, count, kcount, slot = _filtered(wl)
+    nt, N = keep.shape[0], keep.shape[2]
+    rng = np.random.default_rng(4)
+    a = rng.integers(-100, 100, size=(nt, wl.B, N, wl.C)).astype(np.float32)
+    b = rng.integers(-100, 100, size=(nt, wl.B, N, wl.C)).astype(np.float32)
+    wl32 = wl.replace(dtype="f32")
+    p32 = oracle.problem_of(wl32)
+    oa, ob, oab = (oracle.cond_blend(p32, x, keep, idx, count, N) for x in (a, b, a + b))
+    assert np.max(np.abs(oab - (oa + ob))) < 1e-9
+    one = kcount == 1
+    for bb, k in zip(*np.nonzero(one)):
+        t = int(np.nonzero(keep[:, bb, k])[0][0])
+        assert np.array_equal(oa[bb, k], a[t, bb, slot[t, bb, k]].astype(np.float64))
+
+
+def test_tile_mean_pins():
+    wl = wk.by_name("temporal")
+    p = oracle.problem_of(wl.replace(dtype="f32"))
+    nt, L = int(np.prod(wl.num_tiles)), 96
+    const = np.broadcast_to(np.arange(nt, dtype=np.float32)[:, None, None], (nt, wl.B, L)).copy()
+    assert np.allclose(oracle.tile_mean(p, const, L), (nt - 1) / 2, atol=1e-12)
+    same = np.broadcast_to(np.random.default_rng(1).standard_normal((1, wl.B, L), dtype=np.float32),
+                           (nt, wl.B, L)).copy()
+    assert np.allclose(oracle.tile_mean(p, same, L), same[0].astype(np.float64), rtol=1e-14, atol=1e-15)
+    one = oracle.problem_of(wl.replace(dtype="f32", num_tiles=(1, 1, 1), overlap=(0, 0, 0)))
+    x = np.random.default_rng(3).standard_normal((1, wl.B, L), dtype=np.float32)
+    assert np.array_equal(oracle.tile_mean(one, x, L), x[0].astype(np.float64))
