@@ -31,7 +31,10 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "tdp_oracle.c")
-_LIB = os.path.join(_HERE, "liboracle.so")
+_DEFAULT_LIB = os.path.join(_HERE, "liboracle.so")
+# Test hook: point the wrapper at another build of tdp_oracle.c (the mutation tests
+# load deliberately broken copies to check that the pins catch them).
+_LIB = os.environ.get("TDP_ORACLE_LIB") or _DEFAULT_LIB
 _lock = threading.Lock()
 _lib = None
 
@@ -44,12 +47,20 @@ class Problem(ctypes.Structure):
     ]
 
 
+def compile_source(src: str, out: str) -> str:
+    """gcc -O2 -std=c11 -shared: one oracle source file into a shared library."""
+    tmp = out + f".tmp{os.getpid()}"
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-shared", "-fPIC", "-o", tmp, src])
+    os.replace(tmp, out)
+    return out
+
+
 def build(force: bool = False) -> str:
     """Compile tdp_oracle.c into liboracle.so beside it (gcc, C11, -O2)."""
+    if _LIB != _DEFAULT_LIB:
+        return _LIB
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
-        tmp = _LIB + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-O2", "-std=c11", "-shared", "-fPIC", "-o", tmp, _SRC])
-        os.replace(tmp, _LIB)
+        compile_source(_SRC, _LIB)
     return _LIB
 
 
