@@ -214,3 +214,34 @@ def test_large_workload_in_bench_configuration(tdp):
         zc = oracle.blend_cell(p, Yout_h, 0, f, h, w)
         assert_blend_close(Z[0, f, h, w], zc, wl)
     assert np.isfinite(as_f64(Z)).all()
+
+
+def test_parity_wide_rows(tdp):
+    """W above the blend's per-pass cell table (1024 cells): the table is rebuilt per pass."""
+    wl = wk.by_name("tiny").replace(F=2, H=3, W=1100, C=16, dtype="bf16", num_tiles=(1, 1, 5),
+                                    overlap=(0, 0, 8), n_cond=300)
+    X, P, K = wk.make_inputs(wl)
+    _check_path(tdp, wl, X, P, K)
+
+
+def test_parity_many_cond_tokens(tdp):
+    """More conditioning tokens than one compaction pass (16384) holds."""
+    wl = wk.by_name("small").replace(B=2, n_cond=40000)
+    X, P, K = wk.make_inputs(wl)
+    _check_path(tdp, wl, X, P, K)
+
+
+def test_parity_many_tiles(tdp):
+    """2048 tiles: the keep counts stage tile bounds in shared memory in two rounds."""
+    wl = wk.by_name("tiny").replace(F=4, H=64, W=64, C=8, dtype="bf16", num_tiles=(2, 32, 32),
+                                    overlap=(1, 2, 1), n_cond=300)
+    X, P, K = wk.make_inputs(wl)
+    _check_path(tdp, wl, X, P, K)
+
+
+def test_parity_wide_channels(tdp):
+    """4 KB tokens (bf16 C=2048): 256 vectors per token."""
+    wl = wk.by_name("tiny").replace(F=2, H=6, W=10, C=2048, dtype="bf16", num_tiles=(1, 2, 2),
+                                    overlap=(0, 2, 2), n_cond=100)
+    X, P, K = wk.make_inputs(wl)
+    _check_path(tdp, wl, X, P, K)

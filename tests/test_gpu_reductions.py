@@ -87,3 +87,9 @@ def test_reductions_empty(tdp):
                        torch.empty(0, dtype=torch.int32, device="cuda"), e)
     tdp.tdp_tile_mean(plan, 0, e, e)
     torch.cuda.synchronize()
+
+
+def test_cond_blend_many_tiles(tdp):
+    wl = wk.by_name("tiny").replace(F=4, H=64, W=64, C=8, dtype="bf16", num_tiles=(2, 32, 32),
+                                    overlap=(1, 2, 1), n_cond=300)
+    _cond_case(tdp, wl)
