@@ -44,23 +44,25 @@ PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.txt")
 
 # ----------------------------------------------------------------------------- bytes
 def algorithmic_bytes(wl, total_tile_tokens, n_tiles, kept_total=None):
-    """Bytes each step must move at minimum (per batch of the workload).
+    """Bytes each call must move at minimum (per batch of the workload).
 
-    split : read the latent once + write every tile token       (B*T*C*e + B*sumT*C*e)
-    pos   : read positions once + write tile positions           (B*T*24 + B*sumT*24)
+    bounds: read the positions once, write mn / mx                 (B*T*24 + 2*nt*B*12)
+    split : read the latent and positions once, write every tile token and its
+            positions                                               (B*T*(C*e + 24) + B*sumT*(C*e + 24))
     filter: read cond tokens once, write keep/idx/kcount/count and the kept intervals
-    blend : read every tile-output token once + write the latent (B*sumT*C*e + B*T*C*e)
+    blend : read every tile-output token once, write the latent     (B*sumT*C*e + B*T*C*e)
+    The step counts the positions once (the bounds pass re-reads what the split reads).
     """
     B, T, C, e = wl.B, wl.tokens, wl.C, wl.esize
     tot = total_tile_tokens
     N = wl.n_cond
-    split = B * T * C * e + B * tot * C * e
-    pos = B * T * 24 + B * tot * 24 + 2 * n_tiles * B * 3 * 4
+    mnmx = 2 * n_tiles * B * 3 * 4
+    bounds = B * T * 24 + mnmx
+    split = B * T * C * e + B * tot * C * e + B * T * 24 + B * tot * 24
     kept = kept_total if kept_total is not None else 0
     filt = B * N * 24 + n_tiles * B * N * (1 + 4) + n_tiles * B * 4 + B * N * 4 + kept * 24
     blend = B * tot * C * e + B * T * C * e
-    return dict(split=split, pos=pos, filter=filt, blend=blend,
-                split_call=split + pos, step=split + pos + filt + blend)
+    return dict(bounds=bounds, split=split, filter=filt, blend=blend, step=mnmx + split + filt + blend)
 
 
 def config_of(wl, plan_tokens, n_tiles, parallelism):
@@ -188,6 +190,16 @@ def profiled_traffic(kernel):
     return None
 
 
+# ----------------------------------------------------------------------------- ranks
+def max_over_ranks(x: float, device) -> float:
+    """The largest `x` over all ranks of the default process group (every rank calls it)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ----------------------------------------------------------------------------- CPU oracle
 def oracle_step_time(wl, X, P, K):
     """Wall time of one oracle pass (split, bounds, normalise, filter, blend) on one core."""
@@ -248,7 +260,8 @@ def run_ours(args, rank, world, local_rank):
         Y, Q, mn, mx = tdp.alloc_split_outputs(plan, dev)
         keep, idx, count, kcount, Kout = tdp.alloc_filter_outputs(plan, N, dev)
         Z = torch.empty_like(Xd)
-        tdp.tdp_split(plan, Xd, Pd, 1, Y, Q, mn, mx, stream=s)
+        tdp.tdp_pos_bounds(plan, Pd, mn, mx, stream=s)
+        tdp.tdp_split(plan, Xd, Pd, mn, 1, Y, Q, stream=s)
         gen = torch.Generator(device=dev).manual_seed(wl.seed + 7)
         Yout = (Y.float() + wl.sigma * torch.randn(Y.shape, generator=gen, device=dev)).to(torch.bfloat16)
     s.synchronize()
@@ -256,15 +269,18 @@ def run_ours(args, rank, world, local_rank):
     def step(evs=None):
         if evs is not None:
             evs[0].record(s)
-        tdp.tdp_split(plan, Xd, Pd, 1, Y, Q, mn, mx, stream=s)
+        tdp.tdp_pos_bounds(plan, Pd, mn, mx, stream=s)
         if evs is not None:
             evs[1].record(s)
-        tdp.tdp_norm_filter(plan, Kd, N, mn, mx, 1, keep, idx, count, kcount, Kout, stream=s)
+        tdp.tdp_split(plan, Xd, Pd, mn, 1, Y, Q, stream=s)
         if evs is not None:
             evs[2].record(s)
-        tdp.tdp_blend(plan, Yout, Z, stream=s)
+        tdp.tdp_norm_filter(plan, Kd, N, mn, mx, 1, keep, idx, count, kcount, Kout, stream=s)
         if evs is not None:
             evs[3].record(s)
+        tdp.tdp_blend(plan, Yout, Z, stream=s)
+        if evs is not None:
+            evs[4].record(s)
 
     for _ in range(args.warmup):
         step()
@@ -273,7 +289,7 @@ def run_ours(args, rank, world, local_rank):
     ab = algorithmic_bytes(wl, plan.total_tile_tokens, plan.n_tiles, kept_total)
 
     # ---- timed region: exactly K steps, barrier + synchronize on both sides
-    per = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    per = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(gpu_id_for_smi(torch, local_rank)) if rank == 0 else None
     time.sleep(0.3 if sampler else 0)
@@ -293,13 +309,12 @@ def run_ours(args, rank, world, local_rank):
         sampler.stop()
     ms = start.elapsed_time(stop) / args.steps
     if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+        ms = max_over_ranks(ms, dev)
     k_ms = {
-        "split": statistics.mean(e[0].elapsed_time(e[1]) for e in per),
-        "norm_filter": statistics.mean(e[1].elapsed_time(e[2]) for e in per),
-        "blend": statistics.mean(e[2].elapsed_time(e[3]) for e in per),
+        "pos_bounds": statistics.mean(e[0].elapsed_time(e[1]) for e in per),
+        "split": statistics.mean(e[1].elapsed_time(e[2]) for e in per),
+        "norm_filter": statistics.mean(e[2].elapsed_time(e[3]) for e in per),
+        "blend": statistics.mean(e[3].elapsed_time(e[4]) for e in per),
     }
 
     # ---- the other reductions over tiles (outside the headline step): conditioning
@@ -371,7 +386,8 @@ def run_ours(args, rank, world, local_rank):
                 in_ready[j].record(s_in)
             s.wait_event(in_ready[j])
             s.wait_event(out_free[j])
-            tdp.tdp_split(plan, Xb[j], Pb[j], 1, Y, Q, mn, mx, stream=s)
+            tdp.tdp_pos_bounds(plan, Pb[j], mn, mx, stream=s)
+            tdp.tdp_split(plan, Xb[j], Pb[j], mn, 1, Y, Q, stream=s)
             tdp.tdp_norm_filter(plan, Kb[j], N, mn, mx, 1, keep, idx, count, kcount, Kout, stream=s)
             in_free[j].record(s)
             tdp.tdp_blend(plan, Yout, Zb[j], stream=s)
@@ -395,9 +411,7 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize()
         e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
         if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+            e2e_ms = max_over_ranks(e2e_ms, dev)
         e2e = {"value": world * ab["step"] / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": X.nbytes + P.nbytes + K.nbytes, "d2h_bytes_per_step": X.nbytes,
                "ms_per_step": e2e_ms, "steps": args.e2e_steps,
@@ -407,7 +421,8 @@ def run_ours(args, rank, world, local_rank):
         return None
     peak, peak_kind = hbm_peak()
     kern = {}
-    for name, b in (("split", ab["split_call"]), ("norm_filter", ab["filter"]), ("blend", ab["blend"])):
+    for name, b in (("pos_bounds", ab["bounds"]), ("split", ab["split"]), ("norm_filter", ab["filter"]),
+                    ("blend", ab["blend"])):
         gbs = b / (k_ms[name] * 1e-3) / 1e9
         kern[name] = {"ms": k_ms[name], "algorithmic_bytes": b, "GB/s": gbs, "frac": gbs / peak}
     dom = "blend" if k_ms["blend"] >= k_ms["split"] else "split"
@@ -416,8 +431,6 @@ def run_ours(args, rank, world, local_rank):
     roof = {"bound": "hbm", "kernel": dom_kernel, "achieved": kern[dom]["GB/s"], "peak": peak,
             "peak_kind": f"{peak_kind} copy bandwidth", "unit": "GB/s", "frac": kern[dom]["GB/s"] / peak,
             "traffic": traffic, "algorithmic_bytes_per_launch": kern[dom]["algorithmic_bytes"]}
-    if dom == "split":
-        roof["note"] = "tdp_split timed as its three launches (bounds init, bounds, split)"
     value = world * ab["step"] / (ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,

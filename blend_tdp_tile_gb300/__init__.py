@@ -26,7 +26,8 @@ import numpy as np
 __all__ = [
     "TDP_OK", "TDP_F32", "TDP_BF16", "TDP_MAX_TILES_PER_DIM", "TdpError",
     "Plan", "tdp_plan_create", "tdp_plan_info", "tdp_plan_destroy",
-    "tdp_split", "tdp_norm_filter", "tdp_blend", "tdp_cond_blend", "tdp_tile_mean",
+    "tdp_pos_bounds", "tdp_split", "tdp_norm_filter", "tdp_blend", "tdp_cond_blend", "tdp_tile_mean",
+    "tdp_balanced_tile_split", "tdp_tiles_for_size", "tdp_rank_tiles",
     "tdp_status_str", "tdp_last_error_detail",
     "alloc_split_outputs", "alloc_filter_outputs", "LIB_PATH",
 ]
@@ -65,7 +66,9 @@ def _load():
     lib.tdp_plan_info.restype = ctypes.c_int
     lib.tdp_plan_destroy.argtypes = [vp]
     lib.tdp_plan_destroy.restype = None
-    lib.tdp_split.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp]
+    lib.tdp_pos_bounds.argtypes = [vp, vp, vp, vp, vp]
+    lib.tdp_pos_bounds.restype = ctypes.c_int
+    lib.tdp_split.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp]
     lib.tdp_split.restype = ctypes.c_int
     lib.tdp_norm_filter.argtypes = [vp, vp, i32, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp]
     lib.tdp_norm_filter.restype = ctypes.c_int
@@ -75,6 +78,12 @@ def _load():
     lib.tdp_tile_mean.restype = ctypes.c_int
     lib.tdp_blend.argtypes = [vp, vp, vp, vp]
     lib.tdp_blend.restype = ctypes.c_int
+    lib.tdp_balanced_tile_split.argtypes = [i32, ctypes.POINTER(i32), ctypes.POINTER(i32)]
+    lib.tdp_balanced_tile_split.restype = ctypes.c_int
+    lib.tdp_tiles_for_size.argtypes = [i32, i32, i32, ctypes.POINTER(i32)]
+    lib.tdp_tiles_for_size.restype = ctypes.c_int
+    lib.tdp_rank_tiles.argtypes = [vp, i32, i32, vp, ctypes.POINTER(i32)]
+    lib.tdp_rank_tiles.restype = ctypes.c_int
     lib.tdp_status_str.argtypes = [ctypes.c_int]
     lib.tdp_status_str.restype = ctypes.c_char_p
     lib.tdp_last_error_detail.argtypes = []
@@ -160,6 +169,29 @@ def tdp_plan_destroy(plan: Plan):
     plan.close()
 
 
+def tdp_balanced_tile_split(world: int):
+    """(h_tiles, w_tiles) for `world` ranks: the factor pair closest to square, h <= w."""
+    h, w = ctypes.c_int32(), ctypes.c_int32()
+    _check(_lib.tdp_balanced_tile_split(int(world), ctypes.byref(h), ctypes.byref(w)), "tdp_balanced_tile_split")
+    return int(h.value), int(w.value)
+
+
+def tdp_tiles_for_size(L: int, tile_size: int, overlap: int) -> int:
+    """Smallest valid tile count along a dimension of extent L whose tiles fit in tile_size."""
+    n = ctypes.c_int32()
+    _check(_lib.tdp_tiles_for_size(int(L), int(tile_size), int(overlap), ctypes.byref(n)), "tdp_tiles_for_size")
+    return int(n.value)
+
+
+def tdp_rank_tiles(plan: Plan, rank: int, world: int) -> np.ndarray:
+    """Tile ids rank `rank` of `world` runs under round-robin assignment (tile t -> t % world)."""
+    tiles = np.zeros(max(plan.n_tiles, 1), np.int32)
+    n = ctypes.c_int32()
+    _check(_lib.tdp_rank_tiles(plan.handle, int(rank), int(world), tiles.ctypes.data_as(ctypes.c_void_p),
+                               ctypes.byref(n)), "tdp_rank_tiles")
+    return tiles[:n.value].copy()
+
+
 # ------------------------------------------------------------------ marshalling
 def _torch():
     import torch
@@ -200,19 +232,29 @@ def _stream(stream):
     return stream.cuda_stream
 
 
-def tdp_split(plan: Plan, X, P, normalize, Y, Q, mn, mx, stream=None):
-    """Split X [B,F,H,W,C] (and positions P [B,3,T,2]) into tile-major Y (and Q, mn, mx)."""
+def tdp_pos_bounds(plan: Plan, P, mn, mx, stream=None):
+    """Every tile's min start / max end of its generated positions P [B,3,T,2] into mn, mx [nt,B,3]."""
+    torch = _torch()
+    B, T, nt = plan.B, plan.F * plan.H * plan.W, plan.n_tiles
+    i32 = (torch.int32,)
+    _check(_lib.tdp_pos_bounds(plan.handle, _ptr(P, "P", B * 3 * T * 2, i32, 8),
+                               _ptr(mn, "mn", nt * B * 3, i32, 4), _ptr(mx, "mx", nt * B * 3, i32, 4),
+                               _stream(stream)), "tdp_pos_bounds")
+
+
+def tdp_split(plan: Plan, X, P, mn, normalize, Y, Q, stream=None):
+    """Split X [B,F,H,W,C] (and positions P [B,3,T,2], shifted by mn when normalising) into
+    tile-major Y (and Q)."""
     torch = _torch()
     B, T, C, nt, tot = plan.B, plan.F * plan.H * plan.W, plan.C, plan.n_tiles, plan.total_tile_tokens
     lat = _latent_dtypes(plan)
     args = (
         _ptr(X, "X", B * T * C, lat, 16),
         _ptr(P, "P", B * 3 * T * 2, (torch.int32,), 8),
+        _ptr(mn, "mn", nt * B * 3, (torch.int32,), 4),
         int(bool(normalize)),
         _ptr(Y, "Y", B * tot * C, lat, 16),
         _ptr(Q, "Q", B * tot * 6, (torch.int32,), 8),
-        _ptr(mn, "mn", nt * B * 3, (torch.int32,), 4),
-        _ptr(mx, "mx", nt * B * 3, (torch.int32,), 4),
         _stream(stream),
     )
     _check(_lib.tdp_split(plan.handle, *args), "tdp_split")

@@ -197,3 +197,46 @@ extern "C" const char *tdp_last_error_detail(void)
 {
     return g_detail.c_str();
 }
+
+extern "C" tdp_status tdp_balanced_tile_split(int32_t world, int32_t *h_tiles, int32_t *w_tiles)
+{
+    if (world < 1 || !h_tiles || !w_tiles) return tdp_fail(TDP_ERR_INVALID_ARG, "need world >= 1 and outputs");
+    int32_t best = 1;
+    for (int32_t h = 1; (int64_t)h * h <= world; ++h)
+        if (world % h == 0) best = h;    // the largest divisor <= sqrt(world)
+    *h_tiles = best;
+    *w_tiles = world / best;
+    return tdp_ok();
+}
+
+extern "C" tdp_status tdp_tiles_for_size(int32_t L, int32_t tile_size, int32_t overlap, int32_t *num_tiles)
+{
+    if (!num_tiles || L < 1 || tile_size < 1 || overlap < 0)
+        return tdp_fail(TDP_ERR_INVALID_ARG, "need L, tile_size >= 1, overlap >= 0 and an output");
+    const int32_t nmax = L < TDP_MAX_TILES_PER_DIM ? L : TDP_MAX_TILES_PER_DIM;
+    std::string why;
+    for (int32_t n = 1; n <= nmax; ++n) {
+        tdp_dim_geom dg;
+        if (!make_dim(L, n, overlap, &dg, &why)) continue;
+        int32_t largest = 0;
+        for (int32_t i = 0; i < n; ++i) largest = dg.hi[i] - dg.lo[i] > largest ? dg.hi[i] - dg.lo[i] : largest;
+        if (largest <= tile_size) {
+            *num_tiles = n;
+            return tdp_ok();
+        }
+    }
+    return tdp_fail(TDP_ERR_BAD_GEOMETRY, "no valid tile count gives tiles that small");
+}
+
+extern "C" tdp_status tdp_rank_tiles(tdp_plan_t plan, int32_t rank, int32_t world, int32_t *tiles, int32_t *n)
+{
+    if (!plan || !n || world < 1 || rank < 0 || rank >= world)
+        return tdp_fail(TDP_ERR_INVALID_ARG, "need a plan, an output and 0 <= rank < world");
+    int32_t k = 0;
+    for (int32_t t = rank; t < plan->g.nt; t += world) {
+        if (tiles) tiles[k] = t;
+        ++k;
+    }
+    *n = k;
+    return tdp_ok();
+}

@@ -121,6 +121,22 @@ tdp_status tdp_plan_info(tdp_plan_t plan, int32_t *n_tiles, int64_t *total_tile_
 void tdp_plan_destroy(tdp_plan_t plan);
 
 /*
+ * tdp_pos_bounds -- every tile's position extent: minimum start and maximum end
+ * of its generated tokens, per batch item and dimension.
+ * ("Position normalization": each tile's positions are shifted by the minimum
+ *  start of its generated tokens, per batch item and dimension; the maximum
+ *  end is the tile's far edge for the conditioning filter.)
+ *
+ *   P       device [B,3,T,2] int32 generated-token positions, read once.
+ *   mn, mx  device [n_tiles,B,3] int32, written (global coordinates).
+ *   stream  CUDA stream.
+ * Positions are usually fixed by the latent grid: a caller whose positions do not
+ * change between steps may compute mn/mx once and reuse them.
+ */
+tdp_status tdp_pos_bounds(tdp_plan_t plan, const int32_t *P, int32_t *mn, int32_t *mx,
+                          tdp_stream_t stream);
+
+/*
  * tdp_split -- tile split with tile positions and position normalisation.
  * ("What it is": split the patchified latent into tiles, each tile's tokens
  *  go to one transformer call; "Position normalization": each tile's
@@ -129,19 +145,19 @@ void tdp_plan_destroy(tdp_plan_t plan);
  *
  *   X          device [B,F,H,W,C] latent (dtype of the plan), read.
  *   P          device [B,3,T,2] int32 generated-token positions, read; or NULL.
+ *   mn         device [n_tiles,B,3] int32 from tdp_pos_bounds, read when P is set
+ *              and normalize is nonzero (may be NULL otherwise).
  *   normalize  nonzero: Q holds positions minus mn (the page's default,
  *              normalize_positions=True); zero: Q holds the global positions.
  *   Y          device tile-major tiles, B * total_tile_tokens * C elements, written.
  *   Q          device tile-major tile positions, B * total_tile_tokens * 6 int32,
  *              written; NULL exactly when P is NULL.
- *   mn, mx     device [n_tiles,B,3] int32, written: min start / max end over the
- *              tile's generated tokens (global coordinates); NULL exactly when P is NULL.
  *   stream     CUDA stream the work is queued on.
  * Y[t][b][j][:] = X[b, lo_F+f, lo_H+h, lo_W+w, :] for tile-local token j = (f,h,w):
- * a bit-exact copy.  Buffers must not overlap.
+ * a bit-exact copy, each latent element read once.  Buffers must not overlap.
  */
-tdp_status tdp_split(tdp_plan_t plan, const void *X, const int32_t *P, int32_t normalize,
-                     void *Y, int32_t *Q, int32_t *mn, int32_t *mx, tdp_stream_t stream);
+tdp_status tdp_split(tdp_plan_t plan, const void *X, const int32_t *P, const int32_t *mn, int32_t normalize,
+                     void *Y, int32_t *Q, tdp_stream_t stream);
 
 /*
  * tdp_norm_filter -- per-tile conditioning-token filter with normalisation.
@@ -157,7 +173,7 @@ tdp_status tdp_split(tdp_plan_t plan, const void *X, const int32_t *P, int32_t n
  *
  *   K          device [B,3,N,2] int32 conditioning-token intervals, read.
  *   N          tokens per batch item (>= 0; with N = 0 only count is written, all zero).
- *   mn, mx     device [n_tiles,B,3] int32 from tdp_split, read.
+ *   mn, mx     device [n_tiles,B,3] int32 from tdp_pos_bounds, read.
  *   normalize  nonzero: Kout = K - mn[t,b,d]; zero: Kout = K.
  *   keep       device [n_tiles,B,N] uint8, written: 1 if tile t keeps token k of item b.
  *   idx        device [n_tiles,B,N] int32, written: kept k in ascending order,
@@ -235,6 +251,35 @@ tdp_status tdp_tile_mean(tdp_plan_t plan, int64_t L, const void *A, void *out, t
  *   stream CUDA stream.
  */
 tdp_status tdp_blend(tdp_plan_t plan, const void *Yout, void *Z, tdp_stream_t stream);
+
+/*
+ * Plan helpers (host only, no CUDA call).
+ *
+ * tdp_balanced_tile_split -- a height x width tile grid for `world` ranks
+ * ("API / Usage": h_tiles, w_tiles = balanced_tile_split(world size) picks a
+ * balanced 2-D spatial grid over the group; the page does not define it).
+ * Reading taken: the factor pair h * w = world closest to square, h <= w
+ * (video latents are wider than tall).  world >= 1.
+ */
+tdp_status tdp_balanced_tile_split(int32_t world, int32_t *h_tiles, int32_t *w_tiles);
+
+/*
+ * tdp_tiles_for_size -- the tile count along one dimension for a largest tile
+ * size, for callers that think in sizes ("API / Tiling config" contrasts the
+ * count-based TileCountConfig with the size-based VAE TilingConfig).  Returns
+ * in *num_tiles the smallest valid count n (see tdp_plan_create) whose tiles
+ * are all at most tile_size cells long, or TDP_ERR_BAD_GEOMETRY if none is.
+ */
+tdp_status tdp_tiles_for_size(int32_t L, int32_t tile_size, int32_t overlap, int32_t *num_tiles);
+
+/*
+ * tdp_rank_tiles -- the tiles rank `rank` of `world` runs under round-robin
+ * assignment ("What it is": tiles are assigned round-robin, so there may be
+ * more tiles than GPUs: 16 tiles on 4 GPUs is 4 tiles per rank): tile t goes
+ * to rank t % world.  Writes the rank's tile ids in ascending order to `tiles`
+ * (room for n_tiles, may be NULL) and their number to *n.
+ */
+tdp_status tdp_rank_tiles(tdp_plan_t plan, int32_t rank, int32_t world, int32_t *tiles, int32_t *n);
 
 /* Static string naming a status. */
 const char *tdp_status_str(tdp_status status);

@@ -47,7 +47,9 @@ def run_split_filter(tdp, plan, wl, X, P, K, normalize=True, stream=None, positi
     for t in (Y, Q, mn, mx):
         if t is not None:
             fill_sentinel(t)
-    tdp.tdp_split(plan, Xd, Pd, normalize, Y, Q, mn, mx, stream=stream)
+    if positions:
+        tdp.tdp_pos_bounds(plan, Pd, mn, mx, stream=stream)
+    tdp.tdp_split(plan, Xd, Pd, mn, normalize, Y, Q, stream=stream)
     out = dict(Yd=Y, Y=to_host(Y))
     if positions:
         out.update(Q=to_host(Q), mn=to_host(mn), mx=to_host(mx))

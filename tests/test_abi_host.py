@@ -120,8 +120,10 @@ def test_bad_dtype_and_null_args(tdp):
     assert lib.tdp_plan_create(None, ctypes.byref(h)) == 1
     lib.tdp_blend.argtypes = [ctypes.c_void_p] * 4
     assert lib.tdp_blend(None, None, None, None) == 1
-    lib.tdp_split.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32] + [ctypes.c_void_p] * 5
-    assert lib.tdp_split(None, None, None, 1, None, None, None, None, None) == 1
+    lib.tdp_split.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int32] + [ctypes.c_void_p] * 3
+    assert lib.tdp_split(None, None, None, None, 1, None, None, None) == 1
+    lib.tdp_pos_bounds.argtypes = [ctypes.c_void_p] * 5
+    assert lib.tdp_pos_bounds(None, None, None, None, None) == 1
 
 
 @no_gpu_only
@@ -130,15 +132,19 @@ def test_host_validation_before_launch(tdp):
     lib = ctypes.CDLL(tdp.LIB_PATH)
     plan = tdp.tdp_plan_create(1, 3, 8, 12, 16, "f32", (1, 2, 2), (0, 2, 2))
     vp = ctypes.c_void_p
-    lib.tdp_split.argtypes = [vp, vp, vp, ctypes.c_int32, vp, vp, vp, vp, vp]
+    lib.tdp_split.argtypes = [vp, vp, vp, vp, ctypes.c_int32, vp, vp, vp]
+    lib.tdp_pos_bounds.argtypes = [vp, vp, vp, vp, vp]
     lib.tdp_blend.argtypes = [vp, vp, vp, vp]
     lib.tdp_norm_filter.argtypes = [vp, vp, ctypes.c_int32, vp, vp, ctypes.c_int32, vp, vp, vp, vp, vp, vp, vp]
     lib.tdp_cond_blend.argtypes = [vp, ctypes.c_int32, ctypes.c_int32, vp, vp, vp, vp]
     lib.tdp_tile_mean.argtypes = [vp, ctypes.c_int64, vp, vp, vp]
-    # positions half given
-    assert lib.tdp_split(plan.handle, 16, 8, 1, 16, None, None, None, None) == 1
+    # positions without an output for them, and normalising without mn
+    assert lib.tdp_split(plan.handle, 16, 8, 16, 1, 16, None, None) == 1
+    assert lib.tdp_split(plan.handle, 16, 8, None, 1, 16, 8, None) == 1
     # misaligned latent pointer (never dereferenced: refused on the host)
-    assert lib.tdp_split(plan.handle, 24, None, 1, 16, None, None, None, None) == 4
+    assert lib.tdp_split(plan.handle, 24, None, None, 1, 16, None, None) == 4
+    assert lib.tdp_pos_bounds(plan.handle, None, 16, 16, None) == 1
+    assert lib.tdp_pos_bounds(plan.handle, 4, 16, 16, None) == 4
     assert lib.tdp_blend(plan.handle, 16, 40, None) == 4
     assert lib.tdp_blend(plan.handle, None, 16, None) == 1
     assert lib.tdp_norm_filter(plan.handle, None, -1, 16, 16, 1, None, None, 16, None, None, None, None) == 1

@@ -168,7 +168,8 @@ def test_zero_batch(tdp):
     Y, Q, mn, mx = tdp.alloc_split_outputs(plan, "cuda")
     X = torch.empty((0, wl.F, wl.H, wl.W, wl.C), device="cuda")
     P = torch.empty((0, 3, wl.tokens, 2), dtype=torch.int32, device="cuda")
-    tdp.tdp_split(plan, X, P, 1, Y, Q, mn, mx)
+    tdp.tdp_pos_bounds(plan, P, mn, mx)
+    tdp.tdp_split(plan, X, P, mn, 1, Y, Q)
     Z = torch.empty_like(X)
     tdp.tdp_blend(plan, Y, Z)
     torch.cuda.synchronize()
