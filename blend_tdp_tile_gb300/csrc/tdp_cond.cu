@@ -5,8 +5,8 @@
 //                          (reference) positions": weight 1/(tiles that kept it));
 //   tdp_tile_mean_kernel   the audio latent averaged over all tiles ("What it
 //                          is": audio is processed on every tile and averaged).
-// Both are gather form: a thread owns one 16-byte output vector and walks the
-// tiles in ascending order, accumulating in fp32; no atomics, no scratch.
+// Both are gather form and accumulate in fp32 in ascending tile order; no
+// atomics, no scratch.
 #include "tdp.h"
 #include "tdp_device.cuh"
 #include "tdp_internal.h"
@@ -14,7 +14,7 @@
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kTileUnroll = 4;
+constexpr int kTileUnroll = 16;   // tiles whose loads a thread keeps in flight
 
 template <int BF16>
 __device__ __forceinline__ void acc_add(float (&a)[8], const uint4 &y)
@@ -44,34 +44,52 @@ __device__ __forceinline__ uint4 acc_div(const float (&a)[8], float n)
                       __float_as_uint(__fdiv_rn(a[2], n)), __float_as_uint(__fdiv_rn(a[3], n)));
 }
 
-// Thread = output vector (b, k, cv) of out[B, N, C].
+// Warp = one conditioning token (b, k).  Per round of 32 tiles, lane l loads the
+// token's slot in tile t0 + l; a ballot gives the tiles that kept it, in
+// ascending order, and their rows (lanes across the channel vectors) are loaded
+// up to kRowsInFlight at a time and accumulated in that order.
+constexpr int kRowsInFlight = 4;
+
 template <int BF16>
 __global__ void __launch_bounds__(kThreads)
 tdp_cond_blend_kernel(const __grid_constant__ tdp_geom g, int32_t N, int32_t ncap, int32_t CV,
                       const uint4 *__restrict__ Ycond, const int32_t *__restrict__ slot, uint4 *__restrict__ out)
 {
-    const int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (v >= (int64_t)g.B * N * CV) return;
-    const int64_t bk = v / CV;
-    const int32_t cv = (int32_t)(v - bk * CV);
-    const int32_t b = (int32_t)(bk / N), k = (int32_t)(bk - (int64_t)b * N);
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    int32_t n = 0;
-    for (int32_t t0 = 0; t0 < g.nt; t0 += kTileUnroll) {
-        int32_t sl[kTileUnroll];
+    const int32_t lane = threadIdx.x & 31;
+    const int64_t tok = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+    if (tok >= (int64_t)g.B * N) return;                 // warp-uniform
+    const int32_t b = (int32_t)(tok / N), k = (int32_t)(tok - (int64_t)b * N);
+    for (int32_t cv0 = 0; cv0 < CV; cv0 += 32) {
+        const int32_t cv = cv0 + lane;
+        const bool act = cv < CV;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        int32_t n = 0;
+        for (int32_t t0 = 0; t0 < g.nt; t0 += 32) {
+            const int32_t t = t0 + lane;
+            const int32_t sl = t < g.nt ? __ldg(slot + ((int64_t)t * g.B + b) * N + k) : -1;
+            uint32_t m = __ballot_sync(0xffffffffu, sl >= 0 && sl < ncap);
+            while (m) {                                      // warp-uniform
+                uint4 y[kRowsInFlight];
+                int32_t got = 0;
 #pragma unroll
-        for (int u = 0; u < kTileUnroll; ++u)
-            sl[u] = t0 + u < g.nt ? __ldg(slot + ((int64_t)(t0 + u) * g.B + b) * N + k) : -1;
+                for (int u = 0; u < kRowsInFlight; ++u) {
+                    if (m) {
+                        const int32_t j = __ffs(m) - 1;
+                        m &= m - 1;
+                        const int32_t sj = __shfl_sync(0xffffffffu, sl, j);
+                        const int64_t tb = (int64_t)(t0 + j) * g.B + b;
+                        if (act) y[u] = __ldcs(Ycond + (tb * ncap + sj) * CV + cv);
+                        got = u + 1;
+                    }
+                }
 #pragma unroll
-        for (int u = 0; u < kTileUnroll; ++u) {
-            if (sl[u] >= 0 && sl[u] < ncap) {
-                const int64_t tb = (int64_t)(t0 + u) * g.B + b;
-                acc_add<BF16>(acc, __ldcs(Ycond + (tb * ncap + sl[u]) * CV + cv));
-                ++n;
+                for (int u = 0; u < kRowsInFlight; ++u)
+                    if (u < got && act) acc_add<BF16>(acc, y[u]);
+                n += got;
             }
         }
+        if (act) __stcs(out + tok * CV + cv, n > 0 ? acc_div<BF16>(acc, (float)n) : make_uint4(0u, 0u, 0u, 0u));
     }
-    __stcs(out + v, n > 0 ? acc_div<BF16>(acc, (float)n) : make_uint4(0u, 0u, 0u, 0u));
 }
 
 // Thread = output vector of out[B, L].
@@ -107,8 +125,8 @@ extern "C" tdp_status tdp_cond_blend(tdp_plan_t plan, int32_t N, int32_t ncap, c
     if (!tdp_aligned(Ycond, 16) || !tdp_aligned(out, 16) || !tdp_aligned(slot, 4))
         return tdp_fail(TDP_ERR_MISALIGNED, "Ycond and out need 16-byte, slot 4-byte alignment");
     const int32_t CV = (g.C * g.esize) >> 4;
-    const int64_t nvec = (int64_t)g.B * N * CV;
-    const int64_t blocks = (nvec + kThreads - 1) / kThreads;
+    const int64_t warps = (int64_t)g.B * N;                  // one warp per conditioning token
+    const int64_t blocks = (warps + kThreads / 32 - 1) / (kThreads / 32);
     if (blocks > 0x7fffffffLL) return tdp_fail(TDP_ERR_TOO_LARGE, "cond blend grid too large");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const uint4 *y = reinterpret_cast<const uint4 *>(Ycond);
