@@ -15,6 +15,7 @@
 namespace {
 
 constexpr int kSplitThreads = 256;
+constexpr int kSplitUnroll = 4;      // latent vectors each thread loads before storing any
 
 // Block = one latent row (b, f, h).  CV = 16-byte vectors per token.
 __global__ void __launch_bounds__(kSplitThreads)
@@ -48,13 +49,23 @@ tdp_split_kernel(const __grid_constant__ tdp_geom g, const uint4 *__restrict__ X
     // latent: every 16-byte vector of the row is loaded once and stored to each tile
     const int32_t nvec = g.W * CV;
     const uint4 *src = X + gtok * CV;
-    for (int32_t v = threadIdx.x; v < nvec; v += blockDim.x) {
-        const int32_t w = v / CV, cv = v - w * CV;
-        const uint4 x = __ldcs(src + v);
-        const tdp_cover cW = tdp_cover_tab(s_loW, s_hiW, nW, g.W, oW, w);
-        for (int32_t c = 0; c < rc.nc; ++c) {
-            __stcs(Y + (s_tok[c * nW + cW.i0] + w) * CV + cv, x);
-            if (cW.i1 >= 0) __stcs(Y + (s_tok[c * nW + cW.i1] + w) * CV + cv, x);
+    for (int32_t v0 = threadIdx.x; v0 < nvec; v0 += kSplitUnroll * blockDim.x) {
+        uint4 xs[kSplitUnroll];                     // kSplitUnroll loads in flight per thread
+#pragma unroll
+        for (int u = 0; u < kSplitUnroll; ++u) {
+            const int32_t v = v0 + u * blockDim.x;
+            if (v < nvec) xs[u] = __ldcs(src + v);
+        }
+#pragma unroll
+        for (int u = 0; u < kSplitUnroll; ++u) {
+            const int32_t v = v0 + u * blockDim.x;
+            if (v >= nvec) break;
+            const int32_t w = v / CV, cv = v - w * CV;
+            const tdp_cover cW = tdp_cover_tab(s_loW, s_hiW, nW, g.W, oW, w);
+            for (int32_t c = 0; c < rc.nc; ++c) {
+                __stcs(Y + (s_tok[c * nW + cW.i0] + w) * CV + cv, xs[u]);
+                if (cW.i1 >= 0) __stcs(Y + (s_tok[c * nW + cW.i1] + w) * CV + cv, xs[u]);
+            }
         }
     }
     if (!P) return;
@@ -75,7 +86,7 @@ tdp_split_kernel(const __grid_constant__ tdp_geom g, const uint4 *__restrict__ X
                     o.x = (int32_t)((uint32_t)p.x - (uint32_t)m);
                     o.y = (int32_t)((uint32_t)p.y - (uint32_t)m);
                 }
-                __stcs(Q + s_qpos[e] + (int64_t)d * s_Tt[e] + w, o);
+                Q[s_qpos[e] + (int64_t)d * s_Tt[e] + w] = o;   // default policy: neighbouring rows merge in L2
             }
         }
     }
