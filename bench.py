@@ -39,6 +39,8 @@ METRIC = "TDP split+blend effective GB/s (fraction of GB300 HBM peak); latent to
 WORKLOAD = "large"
 FALLBACK_HBM_GBS = 6800.0
 AUDIO_TOKENS = 2048          # synthetic per-tile audio latent for the tile-mean timing
+# kernels one step launches: bounds init + bounds, split, keep + compact, blend
+LAUNCHES_PER_STEP = 6
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.txt")
 
 
@@ -317,6 +319,31 @@ def run_ours(args, rank, world, local_rank):
         "blend": statistics.mean(e[3].elapsed_time(e[4]) for e in per),
     }
 
+    # ---- the same step captured once in a CUDA graph and replayed (launch overhead
+    # of the four calls paid once); reported beside the headline, not instead of it
+    graph = None
+    if rank == 0 and not args.no_graph:
+        with torch.cuda.stream(s):
+            step()
+        s.synchronize()
+        cg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cg, stream=s):
+            step()
+        for _ in range(3):
+            cg.replay()
+        torch.cuda.synchronize()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = max(10, min(args.steps, 500))
+        g0.record(s)
+        with torch.cuda.stream(s):
+            for _ in range(reps):
+                cg.replay()
+        g1.record(s)
+        torch.cuda.synchronize()
+        g_ms = g0.elapsed_time(g1) / reps
+        graph = {"ms_per_step": g_ms, "value": ab["step"] / (g_ms * 1e-3) / 1e9, "unit": "GB/s", "replays": reps}
+        del cg
+
     # ---- the other reductions over tiles (outside the headline step): conditioning
     # outputs averaged over the tiles that kept each token, audio mean over tiles
     extras = None
@@ -441,10 +468,11 @@ def run_ours(args, rank, world, local_rank):
                                                  f"replicas x{world}" if world > 1 else "single GPU"),
         "frac_of_peak": value / world / peak, "latent_tokens_per_s": world * wl.B * wl.tokens / (ms * 1e-3),
         "step_algorithmic_bytes": ab["step"], "kernels": kern, "roofline": roof,
-        "gpu_launches": 5 * args.steps,
+        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
         "clocks": sampler.summary(t0, t1) if sampler else None,
         "e2e": e2e,
         "extra_kernels": extras,
+        "graph_step": graph,
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, X, P, K)
@@ -499,6 +527,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip the timing of the extra reductions")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
