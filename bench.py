@@ -1,9 +1,12 @@
 #!/usr/bin/env python
 """Benchmark of the TDP hot path: tile split (+positions) -> conditioning filter -> blend.
 
-One step = tdp_split, tdp_norm_filter and tdp_blend over the large workload
-(B=1, F=64, H=128, W=192, C=128 bf16; 2x8x8 tiles with overlap (4,16,16);
-16384 conditioning tokens), inputs resident in HBM.  The tile outputs fed to
+One step = the pre-model stage (position bounds, tile split with normalised
+positions, conditioning filter) and the blend over the large workload (B=1,
+F=64, H=128, W=192, C=128 bf16; 2x8x8 tiles with overlap (4,16,16); 16384
+conditioning tokens), inputs resident in HBM.  --path fused (default) runs the
+pre-model stage as one tdp_split_filter call; --path separate as tdp_pos_bounds,
+tdp_split and tdp_norm_filter.  The tile outputs fed to
 the blend are the split tiles plus N(0, 0.05) noise, made once before timing
 (the stand-in for the per-tile transformer, which is not part of the path).
 
@@ -39,8 +42,11 @@ METRIC = "TDP split+blend effective GB/s (fraction of GB300 HBM peak); latent to
 WORKLOAD = "large"
 FALLBACK_HBM_GBS = 6800.0
 AUDIO_TOKENS = 2048          # synthetic per-tile audio latent for the tile-mean timing
-# kernels one step launches: bounds init + bounds, split, keep + compact, blend
-LAUNCHES_PER_STEP = 6
+# kernels one step launches
+LAUNCHES_PER_STEP = {
+    "fused": 4,       # bounds init, bounds, split + filter, blend
+    "separate": 6,    # bounds init, bounds, split, keep, compact, blend
+}
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.txt")
 
 
@@ -170,26 +176,41 @@ def kernel_source_hash(names):
     return h.hexdigest()[:16]
 
 
+_COMMON = ["tdp_device.cuh", "tdp_geom.h", "tdp_internal.h"]
 KERNEL_SOURCES = {
-    "tdp_blend_kernel": ["tdp_blend.cu", "tdp_device.cuh", "tdp_geom.h"],
-    "tdp_split_kernel": ["tdp_split.cu", "tdp_device.cuh", "tdp_geom.h"],
+    "tdp_blend_kernel": ["tdp_blend.cu"] + _COMMON,
+    "tdp_split_kernel": ["tdp_split.cu", "tdp_filter.cuh"] + _COMMON,
+    "tdp_split_filter_kernel": ["tdp_split.cu", "tdp_filter.cuh"] + _COMMON,
+    "tdp_bounds_init_kernel": ["tdp_bounds.cu"] + _COMMON,
+    "tdp_bounds_kernel": ["tdp_bounds.cu"] + _COMMON,
+}
+# the kernels each timed call launches
+CALL_KERNELS = {
+    "tdp_split_filter": ["tdp_bounds_init_kernel", "tdp_bounds_kernel", "tdp_split_filter_kernel"],
+    "tdp_split": ["tdp_split_kernel"],
+    "tdp_blend": ["tdp_blend_kernel"],
 }
 
 
-def profiled_traffic(kernel):
-    """DRAM bytes per launch of `kernel` (read + write) from the committed ncu summary, or
-    None when the kernel's sources changed since the capture (or none was taken)."""
+def profiled_traffic(call):
+    """DRAM bytes (read + write) of one `call`, summed over its kernels, from the committed
+    ncu summary; None when a kernel's sources changed since the capture (or none was taken)."""
+    rows = {}
     try:
         with open(PROFILE_TRAFFIC) as fh:
             for line in fh:
                 parts = line.split()
-                if parts and not line.startswith("#") and parts[0] == kernel:
-                    if parts[1] != kernel_source_hash(KERNEL_SOURCES[kernel]):
-                        return None
-                    return int(parts[2]) + int(parts[3])
-    except (OSError, ValueError, IndexError):
+                if parts and not line.startswith("#"):
+                    rows[parts[0]] = parts
+        total = 0
+        for k in CALL_KERNELS[call]:
+            parts = rows[k]
+            if parts[1] != kernel_source_hash(KERNEL_SOURCES[k]):
+                return None
+            total += int(parts[2]) + int(parts[3])
+        return total
+    except (OSError, ValueError, IndexError, KeyError):
         return None
-    return None
 
 
 # ----------------------------------------------------------------------------- ranks
@@ -268,21 +289,35 @@ def run_ours(args, rank, world, local_rank):
         Yout = (Y.float() + wl.sigma * torch.randn(Y.shape, generator=gen, device=dev)).to(torch.bfloat16)
     s.synchronize()
 
+    fused = args.path == "fused"
+
+    def pre_model(Xs, Ps, Ks):
+        """The pre-model stage (bounds, split, normalisation, filter) on stream s."""
+        if fused:
+            tdp.tdp_split_filter(plan, Xs, Ps, Ks, N, 1, Y, Q, mn, mx, keep, idx, count, kcount, Kout, stream=s)
+        else:
+            tdp.tdp_pos_bounds(plan, Ps, mn, mx, stream=s)
+            tdp.tdp_split(plan, Xs, Ps, mn, 1, Y, Q, stream=s)
+            tdp.tdp_norm_filter(plan, Ks, N, mn, mx, 1, keep, idx, count, kcount, Kout, stream=s)
+
     def step(evs=None):
         if evs is not None:
             evs[0].record(s)
-        tdp.tdp_pos_bounds(plan, Pd, mn, mx, stream=s)
+        if fused:
+            tdp.tdp_split_filter(plan, Xd, Pd, Kd, N, 1, Y, Q, mn, mx, keep, idx, count, kcount, Kout, stream=s)
+        else:
+            tdp.tdp_pos_bounds(plan, Pd, mn, mx, stream=s)
+            if evs is not None:
+                evs[3].record(s)
+            tdp.tdp_split(plan, Xd, Pd, mn, 1, Y, Q, stream=s)
+            if evs is not None:
+                evs[4].record(s)
+            tdp.tdp_norm_filter(plan, Kd, N, mn, mx, 1, keep, idx, count, kcount, Kout, stream=s)
         if evs is not None:
             evs[1].record(s)
-        tdp.tdp_split(plan, Xd, Pd, mn, 1, Y, Q, stream=s)
-        if evs is not None:
-            evs[2].record(s)
-        tdp.tdp_norm_filter(plan, Kd, N, mn, mx, 1, keep, idx, count, kcount, Kout, stream=s)
-        if evs is not None:
-            evs[3].record(s)
         tdp.tdp_blend(plan, Yout, Z, stream=s)
         if evs is not None:
-            evs[4].record(s)
+            evs[2].record(s)
 
     for _ in range(args.warmup):
         step()
@@ -312,12 +347,15 @@ def run_ours(args, rank, world, local_rank):
     ms = start.elapsed_time(stop) / args.steps
     if world > 1:
         ms = max_over_ranks(ms, dev)
-    k_ms = {
-        "pos_bounds": statistics.mean(e[0].elapsed_time(e[1]) for e in per),
-        "split": statistics.mean(e[1].elapsed_time(e[2]) for e in per),
-        "norm_filter": statistics.mean(e[2].elapsed_time(e[3]) for e in per),
-        "blend": statistics.mean(e[3].elapsed_time(e[4]) for e in per),
-    }
+    if fused:
+        k_ms = {"split_filter": statistics.mean(e[0].elapsed_time(e[1]) for e in per)}
+    else:
+        k_ms = {
+            "pos_bounds": statistics.mean(e[0].elapsed_time(e[3]) for e in per),
+            "split": statistics.mean(e[3].elapsed_time(e[4]) for e in per),
+            "norm_filter": statistics.mean(e[4].elapsed_time(e[1]) for e in per),
+        }
+    k_ms["blend"] = statistics.mean(e[1].elapsed_time(e[2]) for e in per)
 
     # ---- the same step captured once in a CUDA graph and replayed (launch overhead
     # of the four calls paid once); reported beside the headline, not instead of it
@@ -413,9 +451,7 @@ def run_ours(args, rank, world, local_rank):
                 in_ready[j].record(s_in)
             s.wait_event(in_ready[j])
             s.wait_event(out_free[j])
-            tdp.tdp_pos_bounds(plan, Pb[j], mn, mx, stream=s)
-            tdp.tdp_split(plan, Xb[j], Pb[j], mn, 1, Y, Q, stream=s)
-            tdp.tdp_norm_filter(plan, Kb[j], N, mn, mx, 1, keep, idx, count, kcount, Kout, stream=s)
+            pre_model(Xb[j], Pb[j], Kb[j])
             in_free[j].record(s)
             tdp.tdp_blend(plan, Yout, Zb[j], stream=s)
             out_ready[j].record(s)
@@ -424,7 +460,7 @@ def run_ours(args, rank, world, local_rank):
                 Zh[j].copy_(Zb[j].view(torch.int16), non_blocking=True)
                 out_free[j].record(s_out)
 
-        for i in range(3):
+        for i in range(8):        # first passes over freshly pinned pages run slow
             e2e_step(i)
         torch.cuda.synchronize()
         if world > 1:
@@ -448,16 +484,21 @@ def run_ours(args, rank, world, local_rank):
         return None
     peak, peak_kind = hbm_peak()
     kern = {}
-    for name, b in (("pos_bounds", ab["bounds"]), ("split", ab["split"]), ("norm_filter", ab["filter"]),
-                    ("blend", ab["blend"])):
-        gbs = b / (k_ms[name] * 1e-3) / 1e9
-        kern[name] = {"ms": k_ms[name], "algorithmic_bytes": b, "GB/s": gbs, "frac": gbs / peak}
-    dom = "blend" if k_ms["blend"] >= k_ms["split"] else "split"
-    dom_kernel = "tdp_blend_kernel" if dom == "blend" else "tdp_split_kernel"
-    traffic = profiled_traffic(dom_kernel)
-    roof = {"bound": "hbm", "kernel": dom_kernel, "achieved": kern[dom]["GB/s"], "peak": peak,
+    call_bytes = {"pos_bounds": ab["bounds"], "split": ab["split"], "norm_filter": ab["filter"],
+                  "split_filter": ab["bounds"] + ab["split"] + ab["filter"], "blend": ab["blend"]}
+    call_name = {"split_filter": "tdp_split_filter", "split": "tdp_split", "blend": "tdp_blend"}
+    for name, t_ms in k_ms.items():
+        b = call_bytes[name]
+        gbs = b / (t_ms * 1e-3) / 1e9
+        kern[name] = {"ms": t_ms, "algorithmic_bytes": b, "GB/s": gbs, "frac": gbs / peak}
+    big = "split_filter" if fused else "split"
+    dom = "blend" if k_ms["blend"] >= k_ms[big] else big
+    call = call_name[dom]
+    roof = {"bound": "hbm", "kernel": call if call != "tdp_split_filter" else
+            "tdp_split_filter (tdp_bounds_init_kernel + tdp_bounds_kernel + tdp_split_filter_kernel)",
+            "kernels": CALL_KERNELS[call], "achieved": kern[dom]["GB/s"], "peak": peak,
             "peak_kind": f"{peak_kind} copy bandwidth", "unit": "GB/s", "frac": kern[dom]["GB/s"] / peak,
-            "traffic": traffic, "algorithmic_bytes_per_launch": kern[dom]["algorithmic_bytes"]}
+            "traffic": profiled_traffic(call), "algorithmic_bytes_per_launch": kern[dom]["algorithmic_bytes"]}
     value = world * ab["step"] / (ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -468,7 +509,7 @@ def run_ours(args, rank, world, local_rank):
                                                  f"replicas x{world}" if world > 1 else "single GPU"),
         "frac_of_peak": value / world / peak, "latent_tokens_per_s": world * wl.B * wl.tokens / (ms * 1e-3),
         "step_algorithmic_bytes": ab["step"], "kernels": kern, "roofline": roof,
-        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "gpu_launches": LAUNCHES_PER_STEP[args.path] * args.steps, "path": args.path,
         "clocks": sampler.summary(t0, t1) if sampler else None,
         "e2e": e2e,
         "extra_kernels": extras,
@@ -523,11 +564,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD, choices=[w.name for w in wk.WORKLOADS])
-    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--e2e-steps", type=int, default=60)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip the timing of the extra reductions")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
+    ap.add_argument("--path", choices=["fused", "separate"], default="fused",
+                    help="pre-model stage as one tdp_split_filter call, or as three calls")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

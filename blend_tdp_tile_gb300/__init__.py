@@ -26,7 +26,8 @@ import numpy as np
 __all__ = [
     "TDP_OK", "TDP_F32", "TDP_BF16", "TDP_MAX_TILES_PER_DIM", "TdpError",
     "Plan", "tdp_plan_create", "tdp_plan_info", "tdp_plan_destroy",
-    "tdp_pos_bounds", "tdp_split", "tdp_norm_filter", "tdp_blend", "tdp_cond_blend", "tdp_tile_mean",
+    "tdp_pos_bounds", "tdp_split", "tdp_norm_filter", "tdp_split_filter", "tdp_blend", "tdp_cond_blend",
+    "tdp_tile_mean",
     "tdp_balanced_tile_split", "tdp_tiles_for_size", "tdp_rank_tiles",
     "tdp_status_str", "tdp_last_error_detail",
     "alloc_split_outputs", "alloc_filter_outputs", "LIB_PATH",
@@ -72,6 +73,8 @@ def _load():
     lib.tdp_split.restype = ctypes.c_int
     lib.tdp_norm_filter.argtypes = [vp, vp, i32, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp]
     lib.tdp_norm_filter.restype = ctypes.c_int
+    lib.tdp_split_filter.argtypes = [vp, vp, vp, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.tdp_split_filter.restype = ctypes.c_int
     lib.tdp_cond_blend.argtypes = [vp, i32, i32, vp, vp, vp, vp]
     lib.tdp_cond_blend.restype = ctypes.c_int
     lib.tdp_tile_mean.argtypes = [vp, ctypes.c_int64, vp, vp, vp]
@@ -282,6 +285,35 @@ def tdp_norm_filter(plan: Plan, K, N, mn, mx, normalize, keep, idx, count, kcoun
         _stream(stream),
     )
     _check(_lib.tdp_norm_filter(plan.handle, *args), "tdp_norm_filter")
+
+
+def tdp_split_filter(plan: Plan, X, P, K, N, normalize, Y, Q, mn, mx, keep, idx, count, kcount, Kout,
+                     slot=None, stream=None):
+    """tdp_pos_bounds + tdp_split + tdp_norm_filter in one call (three launches): the same
+    outputs, bit for bit."""
+    torch = _torch()
+    B, T, C, nt, tot = plan.B, plan.F * plan.H * plan.W, plan.C, plan.n_tiles, plan.total_tile_tokens
+    N = int(N)
+    lat = _latent_dtypes(plan)
+    i32 = (torch.int32,)
+    args = (
+        _ptr(X, "X", B * T * C, lat, 16),
+        _ptr(P, "P", B * 3 * T * 2, i32, 8),
+        _ptr(K, "K", B * 3 * N * 2, i32, 8), N,
+        int(bool(normalize)),
+        _ptr(Y, "Y", B * tot * C, lat, 16),
+        _ptr(Q, "Q", B * tot * 6, i32, 8),
+        _ptr(mn, "mn", nt * B * 3, i32, 4),
+        _ptr(mx, "mx", nt * B * 3, i32, 4),
+        _ptr(keep, "keep", nt * B * N, (torch.uint8,), 1),
+        _ptr(idx, "idx", nt * B * N, i32, 4),
+        _ptr(count, "count", nt * B, i32, 4),
+        _ptr(kcount, "kcount", B * N, i32, 4),
+        _ptr(Kout, "Kout", nt * B * 3 * N * 2, i32, 8),
+        _ptr(slot, "slot", nt * B * N, i32, 4),
+        _stream(stream),
+    )
+    _check(_lib.tdp_split_filter(plan.handle, *args), "tdp_split_filter")
 
 
 def tdp_cond_blend(plan: Plan, N, ncap, Ycond, slot, out, stream=None):

@@ -94,6 +94,7 @@ tdp_blend_kernel(const __grid_constant__ tdp_geom g, int32_t cv_shift, const uin
     __shared__ int64_t s_tok[TDP_MAX_COMBOS * TDP_MAX_TILES_PER_DIM];
     __shared__ tdp_wcell s_w[kWTab];
     __shared__ int32_t s_loW[TDP_MAX_TILES_PER_DIM], s_hiW[TDP_MAX_TILES_PER_DIM];
+    tdp_pdl_trigger();
     for (int32_t i = threadIdx.x; i < g.d[2].n; i += blockDim.x) {
         s_loW[i] = g.d[2].lo[i];
         s_hiW[i] = g.d[2].hi[i];
@@ -112,6 +113,8 @@ tdp_blend_kernel(const __grid_constant__ tdp_geom g, int32_t cv_shift, const uin
     float rFH[TDP_MAX_COMBOS];
 #pragma unroll
     for (int c = 0; c < TDP_MAX_COMBOS; ++c) rFH[c] = c < nc ? rc.rFH[c] : 0.0f;
+
+    tdp_pdl_wait();                                   // Yout written by the work before
 
     for (int32_t wbase = 0; wbase < g.W; wbase += kWTab) {
         const int32_t wn = min(kWTab, g.W - wbase);
@@ -173,11 +176,9 @@ extern "C" tdp_status tdp_blend(tdp_plan_t plan, const void *Yout, void *Z, tdp_
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const uint4 *y = reinterpret_cast<const uint4 *>(Yout);
     uint4 *z = reinterpret_cast<uint4 *>(Z);
-    if (g.dtype == TDP_BF16)
-        tdp_blend_kernel<1><<<rows, kBlendThreads, 0, s>>>(g, cv_shift, y, z);
-    else
-        tdp_blend_kernel<0><<<rows, kBlendThreads, 0, s>>>(g, cv_shift, y, z);
-    const cudaError_t err = cudaGetLastError();
+    cudaError_t err = g.dtype == TDP_BF16 ? tdp_launch(true, tdp_blend_kernel<1>, rows, kBlendThreads, s, g, cv_shift, y, z)
+                                          : tdp_launch(true, tdp_blend_kernel<0>, rows, kBlendThreads, s, g, cv_shift, y, z);
+    if (err == cudaSuccess) err = cudaGetLastError();
     if (err != cudaSuccess) return tdp_fail(TDP_ERR_CUDA, cudaGetErrorString(err));
     return tdp_ok();
 }

@@ -5,10 +5,14 @@
 // tile's far edge for the conditioning filter).
 //
 // Two launches on the caller's stream:
-//   1. tdp_bounds_init_kernel  mn = INT32_MAX, mx = INT32_MIN
+//   1. tdp_bounds_init_kernel  mn = INT32_MAX, mx = INT32_MIN (a plain launch: it starts
+//                              once all earlier work in the stream has completed)
 //   2. tdp_bounds_kernel       per (batch, frame, 8 rows; one warp per row): min start /
 //                              max end of every tile's generated tokens in those rows,
-//                              positions read once, folded into mn/mx with atomics
+//                              positions read once, folded into mn/mx with atomics.
+//                              A programmatic dependent launch behind the init kernel:
+//                              the row reductions, which read only the positions, run
+//                              while the init kernel finishes; the atomics wait for it.
 #include <climits>
 
 #include "tdp.h"
@@ -21,6 +25,8 @@ constexpr int kBoundsThreads = 256;
 
 __global__ void tdp_bounds_init_kernel(int32_t *__restrict__ mn, int32_t *__restrict__ mx, int32_t n)
 {
+    tdp_pdl_trigger();
+    tdp_pdl_wait();
     for (int32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
         mn[i] = INT_MAX;
         mx[i] = INT_MIN;
@@ -43,6 +49,7 @@ tdp_bounds_kernel(const __grid_constant__ tdp_geom g, const int2 *__restrict__ P
 {
     __shared__ int32_t s_mn[kBoundsRows][TDP_MAX_TILES_PER_DIM][3];
     __shared__ int32_t s_mx[kBoundsRows][TDP_MAX_TILES_PER_DIM][3];
+    tdp_pdl_trigger();
     const int32_t nchunk = (g.H + kBoundsRows - 1) / kBoundsRows;
     const int32_t chunk = blockIdx.x % nchunk;
     const int32_t f = (blockIdx.x / nchunk) % g.F;
@@ -94,6 +101,9 @@ tdp_bounds_kernel(const __grid_constant__ tdp_geom g, const int2 *__restrict__ P
         }
     }
     __syncthreads();
+    // Positions were read before the wait: this kernel is only launched right behind
+    // tdp_bounds_init_kernel, a plain launch, so every earlier writer of P has completed.
+    tdp_pdl_wait();                                   // mn / mx initialised
     // combine the block's rows per (H-tile, W-tile, dim) and flush
     const int32_t iHa = tdp_cover_1d(g.d[1], h0).i0;
     const tdp_cover cHz = tdp_cover_1d(g.d[1], h1 - 1);
@@ -121,6 +131,17 @@ tdp_bounds_kernel(const __grid_constant__ tdp_geom g, const int2 *__restrict__ P
 
 }  // namespace
 
+cudaError_t tdp_launch_bounds(const tdp_geom &g, const int32_t *P, int32_t *mn, int32_t *mx, cudaStream_t s)
+{
+    const int32_t n = g.nt * g.B * 3;
+    cudaError_t err = tdp_launch(false, tdp_bounds_init_kernel, (unsigned)((n + 255) / 256), 256, s, mn, mx, n);
+    const int64_t blocks = (int64_t)g.B * g.F * ((g.H + kBoundsRows - 1) / kBoundsRows);
+    if (err == cudaSuccess)
+        err = tdp_launch(true, tdp_bounds_kernel, (unsigned)blocks, kBoundsThreads, s, g,
+                         reinterpret_cast<const int2 *>(P), mn, mx);
+    return err;
+}
+
 extern "C" tdp_status tdp_pos_bounds(tdp_plan_t plan, const int32_t *P, int32_t *mn, int32_t *mx,
                                      tdp_stream_t stream)
 {
@@ -130,12 +151,8 @@ extern "C" tdp_status tdp_pos_bounds(tdp_plan_t plan, const int32_t *P, int32_t 
     if (!P || !mn || !mx) return tdp_fail(TDP_ERR_INVALID_ARG, "null P, mn or mx");
     if (!tdp_aligned(P, 8) || !tdp_aligned(mn, 4) || !tdp_aligned(mx, 4))
         return tdp_fail(TDP_ERR_MISALIGNED, "P needs 8-byte and mn, mx 4-byte alignment");
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int32_t n = g.nt * g.B * 3;
-    tdp_bounds_init_kernel<<<(n + 255) / 256, 256, 0, s>>>(mn, mx, n);
-    const int64_t blocks = (int64_t)g.B * g.F * ((g.H + kBoundsRows - 1) / kBoundsRows);
-    tdp_bounds_kernel<<<(unsigned)blocks, kBoundsThreads, 0, s>>>(g, reinterpret_cast<const int2 *>(P), mn, mx);
-    const cudaError_t err = cudaGetLastError();
+    cudaError_t err = tdp_launch_bounds(g, P, mn, mx, reinterpret_cast<cudaStream_t>(stream));
+    if (err == cudaSuccess) err = cudaGetLastError();
     if (err != cudaSuccess) return tdp_fail(TDP_ERR_CUDA, cudaGetErrorString(err));
     return tdp_ok();
 }

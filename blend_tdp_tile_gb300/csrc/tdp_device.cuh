@@ -143,3 +143,15 @@ __device__ __forceinline__ uint32_t tdp_pack_bf16x2(float lo, float hi)
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t *>(&v);
 }
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel of the library lets the next
+// kernel in its stream launch early (tdp_pdl_trigger at its start) and waits
+// for the kernel before it to complete, with its memory visible, before it
+// touches global memory that kernel may write (tdp_pdl_wait).  The work before
+// the wait is limited to kernel parameters and shared memory, except where a
+// kernel is launched only behind a kernel of this library whose own wait comes
+// first (stated at each such kernel).  Both are no-ops for a plain launch.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tdp_pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void tdp_pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }

@@ -14,3 +14,34 @@ static inline bool tdp_aligned(const void *p, uintptr_t a)
 {
     return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
 }
+
+#ifdef __CUDACC__
+#include <cuda_runtime.h>
+
+#include <utility>
+
+// Launch `kernel` on stream `s`; with `pdl` set, as a programmatic dependent
+// launch: it may start once every block of the kernel before it in the stream
+// has run griddepcontrol.launch_dependents, and orders its own global-memory
+// work behind that kernel with griddepcontrol.wait.
+template <typename... KArgs, typename... Args>
+static inline cudaError_t tdp_launch(bool pdl, void (*kernel)(KArgs...), unsigned grid, unsigned block,
+                                     cudaStream_t s, Args &&...args)
+{
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// tdp_bounds_init_kernel (plain launch) then tdp_bounds_kernel (dependent launch)
+// on stream s: mn / mx of every (tile, batch item, dim).  Arguments checked by the caller.
+cudaError_t tdp_launch_bounds(const tdp_geom &g, const int32_t *P, int32_t *mn, int32_t *mx, cudaStream_t s);
+#endif

@@ -17,44 +17,21 @@
 //      with one scan of a (sub-chunk, warp) count table, writes idx, the
 //      shifted intervals and the slots, and pads its own range of idx with -1.
 #include "tdp.h"
-#include "tdp_device.cuh"
+#include "tdp_filter.cuh"
 #include "tdp_internal.h"
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr int kSub = 16;                          // tokens per thread and chunk
-constexpr int kChunk = kThreads * kSub;           // tokens per (tile, batch item) block
-constexpr int kCountTok = 64;                     // tokens per keep-count block
-constexpr int kCountGroups = kThreads / kCountTok;
-constexpr int kTileStage = 1024;                  // tile bounds staged in shared memory at once
-
-// Keep rule: the interval overlaps the tile's extent in all three dimensions
-// ([max(s, mn), min(e, mx)) non-empty), or its time start is negative.
-__device__ __forceinline__ bool tdp_keeps(const int2 (&k)[3], const int32_t (&lo)[3], const int32_t (&hi)[3])
-{
-    bool inside = true;
-#pragma unroll
-    for (int d = 0; d < 3; ++d) inside &= max(k[d].x, lo[d]) < min(k[d].y, hi[d]);
-    return inside || k[0].x < 0;
-}
-
-__device__ __forceinline__ void load_bounds(const int32_t *mn, const int32_t *mx, int64_t tb, int32_t (&lo)[3],
-                                            int32_t (&hi)[3])
-{
-#pragma unroll
-    for (int d = 0; d < 3; ++d) {
-        lo[d] = __ldg(mn + tb * 3 + d);
-        hi[d] = __ldg(mx + tb * 3 + d);
-    }
-}
+using namespace tdp_filt;
 
 __global__ void __launch_bounds__(kThreads)
 tdp_keep_kernel(const __grid_constant__ tdp_geom g, const int2 *__restrict__ K, int32_t N, int32_t nchunk,
                 const int32_t *__restrict__ mn, const int32_t *__restrict__ mx, uint8_t *__restrict__ keep,
                 int32_t *__restrict__ kcount)
 {
+    __shared__ kcount_smem sm;
+    tdp_pdl_trigger();
+    tdp_pdl_wait();
     const int64_t nkeep = (int64_t)g.nt * g.B * nchunk;
     if ((int64_t)blockIdx.x < nkeep) {
         // ---- keep bytes of (t, b), chunk c
@@ -69,51 +46,12 @@ tdp_keep_kernel(const __grid_constant__ tdp_geom g, const int2 *__restrict__ K, 
             const int32_t k = c * kChunk + j * kThreads + threadIdx.x;
             if (k < N) {
                 const int2 kv[3] = {__ldg(Kb + k), __ldg(Kb + (int64_t)N + k), __ldg(Kb + 2 * (int64_t)N + k)};
-                keep[tb * N + k] = tdp_keeps(kv, lo, hi) ? 1 : 0;
+                keep[tb * N + k] = keeps(kv, lo, hi) ? 1 : 0;
             }
         }
         return;
     }
-    // ---- kcount[b, k]: block = (b, kCountTok tokens); thread (group, token) tests tiles
-    // t = group mod kCountGroups against bounds staged in shared memory
-    __shared__ int32_t s_lo[kTileStage][3], s_hi[kTileStage][3];
-    __shared__ int32_t s_cnt[kCountGroups][kCountTok];
-    const int32_t nkb = (N + kCountTok - 1) / kCountTok;
-    const int32_t blk = (int32_t)(blockIdx.x - nkeep);
-    const int32_t b = blk / nkb;
-    const int32_t tok = threadIdx.x % kCountTok, grp = threadIdx.x / kCountTok;
-    const int32_t k = (blk - b * nkb) * kCountTok + tok;
-    const int2 *Kb = K + (int64_t)b * 3 * N;
-    int2 kv[3] = {make_int2(0, 0), make_int2(0, 0), make_int2(0, 0)};
-    if (k < N) {
-#pragma unroll
-        for (int d = 0; d < 3; ++d) kv[d] = __ldg(Kb + (int64_t)d * N + k);
-    }
-    int32_t cnt = 0;
-    for (int32_t u0 = 0; u0 < g.nt; u0 += kTileStage) {
-        const int32_t un = min(kTileStage, g.nt - u0);
-        __syncthreads();   // previous readers of s_lo / s_hi are done
-        for (int32_t i = threadIdx.x; i < un * 3; i += blockDim.x) {
-            const int32_t u = i / 3, d = i - u * 3;
-            const int64_t r = ((int64_t)(u0 + u) * g.B + b) * 3 + d;
-            s_lo[u][d] = __ldg(mn + r);
-            s_hi[u][d] = __ldg(mx + r);
-        }
-        __syncthreads();
-        for (int32_t u = grp; u < un; u += kCountGroups) {        // warp-uniform: shared broadcast
-            const int32_t a[3] = {s_lo[u][0], s_lo[u][1], s_lo[u][2]};
-            const int32_t z[3] = {s_hi[u][0], s_hi[u][1], s_hi[u][2]};
-            cnt += tdp_keeps(kv, a, z) ? 1 : 0;
-        }
-    }
-    s_cnt[grp][tok] = cnt;
-    __syncthreads();
-    if (grp == 0 && k < N) {
-        int32_t sum = 0;
-#pragma unroll
-        for (int i = 0; i < kCountGroups; ++i) sum += s_cnt[i][tok];
-        kcount[(int64_t)b * N + k] = sum;
-    }
+    kcount_block(g, K, N, mn, mx, kcount, (int32_t)(blockIdx.x - nkeep), sm);
 }
 
 // Sum over the block of two values (every thread calls it).
@@ -143,12 +81,12 @@ tdp_compact_kernel(const __grid_constant__ tdp_geom g, const int2 *__restrict__ 
                    int32_t *__restrict__ idx, int32_t *__restrict__ count, int2 *__restrict__ Kout,
                    int32_t *__restrict__ slot)
 {
-    __shared__ int32_t s_sum[kWarps][2];
-    __shared__ int32_t s_off[kSub][kWarps];
+    __shared__ compact_smem sm;
+    tdp_pdl_trigger();
+    tdp_pdl_wait();
     const int64_t tb = blockIdx.x / nchunk;
     const int32_t c = (int32_t)(blockIdx.x - tb * nchunk);
     const int32_t b = (int32_t)(tb % g.B);
-    const int32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint8_t *krow = keep + tb * N;
     const int32_t k0 = c * kChunk;
 
@@ -169,74 +107,22 @@ tdp_compact_kernel(const __grid_constant__ tdp_geom g, const int2 *__restrict__ 
             before += i < k0 ? n : 0;
         }
     }
-    block_sum2(before, total, s_sum);
+    block_sum2(before, total, sm.sum);
 
-    // ---- this chunk: ballots per (sub-chunk, warp), one scan in (j, warp) order
+    // ---- this chunk: ballots per (sub-chunk, warp), offsets from one scan
     uint32_t ballots[kSub];
 #pragma unroll
     for (int j = 0; j < kSub; ++j) {
         const int32_t k = k0 + j * kThreads + threadIdx.x;
         ballots[j] = __ballot_sync(0xffffffffu, k < N && __ldg(krow + k) != 0);
     }
-    if (lane < kSub) {
-        uint32_t mine = 0;
-#pragma unroll
-        for (int j = 0; j < kSub; ++j) mine = lane == j ? ballots[j] : mine;
-        s_off[lane][warp] = __popc(mine);
-    }
-    __syncthreads();
-    if (warp == 0) {
-        // lane l < kSub owns row j = l of the table
-        int32_t row[kWarps];
-        int32_t sum = 0;
-        if (lane < kSub) {
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                row[w] = s_off[lane][w];
-                sum += row[w];
-            }
-        }
-        int32_t incl = sum;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const int32_t v = __shfl_up_sync(0xffffffffu, incl, d);
-            if (lane >= d) incl += v;
-        }
-        if (lane < kSub) {
-            int32_t run = before + incl - sum;
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                s_off[lane][w] = run;
-                run += row[w];
-            }
-        }
-    }
-    __syncthreads();
-
-    int32_t lo[3] = {0, 0, 0};
+    chunk_offsets(ballots, before, sm);
+    int32_t shift[3] = {0, 0, 0};
     if (normalize) {
 #pragma unroll
-        for (int d = 0; d < 3; ++d) lo[d] = __ldg(mn + tb * 3 + d);
+        for (int d = 0; d < 3; ++d) shift[d] = __ldg(mn + tb * 3 + d);
     }
-    const int2 *Kb = K + (int64_t)b * 3 * N;
-    const uint32_t lt_mask = (1u << lane) - 1u;
-#pragma unroll
-    for (int j = 0; j < kSub; ++j) {
-        const int32_t k = k0 + j * kThreads + threadIdx.x;
-        const bool kept = (ballots[j] >> lane) & 1u;
-        const int32_t pos = s_off[j][warp] + __popc(ballots[j] & lt_mask);
-        if (slot && k < N) slot[tb * N + k] = kept ? pos : -1;
-        if (kept) {
-            idx[tb * N + pos] = k;
-#pragma unroll
-            for (int d = 0; d < 3; ++d) {
-                int2 o = __ldg(Kb + (int64_t)d * N + k);
-                o.x = (int32_t)((uint32_t)o.x - (uint32_t)lo[d]);
-                o.y = (int32_t)((uint32_t)o.y - (uint32_t)lo[d]);
-                Kout[(tb * 3 + d) * N + pos] = o;
-            }
-        }
-    }
+    chunk_write(K + (int64_t)b * 3 * N, N, tb, k0, ballots, shift, sm, idx, Kout, slot);
     // ---- idx past the total count: -1, over this chunk's range of positions
     for (int32_t p = max(total, k0) + threadIdx.x; p < min(N, k0 + kChunk); p += blockDim.x) idx[tb * N + p] = -1;
     if (c == 0 && threadIdx.x == 0) count[tb] = total;
@@ -260,6 +146,7 @@ extern "C" tdp_status tdp_norm_filter(tdp_plan_t plan, const int32_t *K, int32_t
         (N > 0 && (!tdp_aligned(K, 8) || !tdp_aligned(Kout, 8) || !tdp_aligned(idx, 4) ||
                    !tdp_aligned(kcount, 4) || !tdp_aligned(slot, 4))))
         return tdp_fail(TDP_ERR_MISALIGNED, "K, Kout need 8-byte and int32 buffers 4-byte alignment");
+    using namespace tdp_filt;
     const int32_t nchunk = N > 0 ? (N + kChunk - 1) / kChunk : 1;
     const int64_t nkeep = (int64_t)g.nt * g.B * nchunk;
     const int64_t blocks1 = nkeep + (int64_t)g.B * ((N + kCountTok - 1) / kCountTok);
@@ -267,11 +154,14 @@ extern "C" tdp_status tdp_norm_filter(tdp_plan_t plan, const int32_t *K, int32_t
         return tdp_fail(TDP_ERR_TOO_LARGE, "filter grid too large");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int2 *k2 = reinterpret_cast<const int2 *>(K);
+    cudaError_t err = cudaSuccess;
     if (N > 0)
-        tdp_keep_kernel<<<(unsigned)blocks1, kThreads, 0, s>>>(g, k2, N, nchunk, mn, mx, keep, kcount);
-    tdp_compact_kernel<<<(unsigned)nkeep, kThreads, 0, s>>>(g, k2, N, nchunk, mn, normalize, keep, idx, count,
-                                                             reinterpret_cast<int2 *>(Kout), slot);
-    const cudaError_t err = cudaGetLastError();
+        err = tdp_launch(true, tdp_keep_kernel, (unsigned)blocks1, kThreads, s, g, k2, N, nchunk, mn, mx, keep,
+                         kcount);
+    if (err == cudaSuccess)
+        err = tdp_launch(true, tdp_compact_kernel, (unsigned)nkeep, kThreads, s, g, k2, N, nchunk, mn, normalize,
+                         static_cast<const uint8_t *>(keep), idx, count, reinterpret_cast<int2 *>(Kout), slot);
+    if (err == cudaSuccess) err = cudaGetLastError();
     if (err != cudaSuccess) return tdp_fail(TDP_ERR_CUDA, cudaGetErrorString(err));
     return tdp_ok();
 }

@@ -193,6 +193,30 @@ tdp_status tdp_norm_filter(tdp_plan_t plan, const int32_t *K, int32_t N,
                            int32_t *Kout, int32_t *slot, tdp_stream_t stream);
 
 /*
+ * tdp_split_filter -- the whole pre-model stage of one TDP forward in one call:
+ * tdp_pos_bounds, tdp_split and tdp_norm_filter with the same arguments and
+ * bit-identical results, in three launches instead of five.
+ * ("What it is", "Position normalization", "Shared negative (reference)
+ *  positions": split the latent into tiles, shift each tile's positions by
+ *  its offset, and give each tile the conditioning tokens it keeps.)
+ *
+ *   X, Y, normalize     as for tdp_split.
+ *   P, Q                as for tdp_split, both required (the bounds need P).
+ *   mn, mx              device [n_tiles,B,3] int32, written as by tdp_pos_bounds.
+ *   K, N, keep, idx, count, kcount, Kout, slot
+ *                       as for tdp_norm_filter (slot may be NULL).
+ *   stream              CUDA stream.
+ * The copy of the latent overlaps the bounds and the filter overlaps the copy:
+ * the kernels use programmatic dependent launch, ordered so that each reads
+ * only what the work before it in the stream has finished writing.  Buffers
+ * must not overlap one another.
+ */
+tdp_status tdp_split_filter(tdp_plan_t plan, const void *X, const int32_t *P, const int32_t *K, int32_t N,
+                            int32_t normalize, void *Y, int32_t *Q, int32_t *mn, int32_t *mx, uint8_t *keep,
+                            int32_t *idx, int32_t *count, int32_t *kcount, int32_t *Kout, int32_t *slot,
+                            tdp_stream_t stream);
+
+/*
  * tdp_cond_blend -- average each conditioning token's per-tile outputs over the
  * tiles that kept it.
  * ("Shared negative (reference) positions": a token kept by several tiles has

@@ -38,7 +38,9 @@ def fill_sentinel(t):
     return t
 
 
-def run_split_filter(tdp, plan, wl, X, P, K, normalize=True, stream=None, positions=True):
+def run_split_filter(tdp, plan, wl, X, P, K, normalize=True, stream=None, positions=True, fused=False):
+    """Bounds, split and filter on the GPU, every output pre-filled with a sentinel.
+    fused=False: tdp_pos_bounds + tdp_split + tdp_norm_filter; fused=True: tdp_split_filter."""
     import torch
     dev = "cuda"
     Xd = to_dev(X)
@@ -47,23 +49,30 @@ def run_split_filter(tdp, plan, wl, X, P, K, normalize=True, stream=None, positi
     for t in (Y, Q, mn, mx):
         if t is not None:
             fill_sentinel(t)
+    N = K.shape[2]
     if positions:
-        tdp.tdp_pos_bounds(plan, Pd, mn, mx, stream=stream)
-    tdp.tdp_split(plan, Xd, Pd, mn, normalize, Y, Q, stream=stream)
-    out = dict(Yd=Y, Y=to_host(Y))
-    if positions:
-        out.update(Q=to_host(Q), mn=to_host(mn), mx=to_host(mx))
-        N = K.shape[2]
         keep, idx, count, kcount, Kout, slot = tdp.alloc_filter_outputs(plan, N, dev, slot=True)
         for t in (keep, idx, count, kcount, Kout, slot):
             fill_sentinel(t)
-        tdp.tdp_norm_filter(plan, to_dev(K), N, mn, mx, normalize, keep, idx, count, kcount, Kout,
-                            slot, stream=stream)
-        out.update(keep=to_host(keep), idx=to_host(idx), count=to_host(count),
-                   kcount=to_host(kcount), Kout=to_host(Kout), slot=to_host(slot), slotd=slot)
+    if fused:
+        assert positions
+        tdp.tdp_split_filter(plan, Xd, Pd, to_dev(K), N, normalize, Y, Q, mn, mx, keep, idx, count, kcount,
+                             Kout, slot, stream=stream)
+    else:
+        if positions:
+            tdp.tdp_pos_bounds(plan, Pd, mn, mx, stream=stream)
+        tdp.tdp_split(plan, Xd, Pd, mn, normalize, Y, Q, stream=stream)
+        if positions:
+            tdp.tdp_norm_filter(plan, to_dev(K), N, mn, mx, normalize, keep, idx, count, kcount, Kout,
+                                slot, stream=stream)
     if stream is not None:
         stream.synchronize()
     torch.cuda.synchronize()
+    out = dict(Yd=Y, Y=to_host(Y))
+    if positions:
+        out.update(Q=to_host(Q), mn=to_host(mn), mx=to_host(mx))
+        out.update(keep=to_host(keep), idx=to_host(idx), count=to_host(count),
+                   kcount=to_host(kcount), Kout=to_host(Kout), slot=to_host(slot), slotd=slot)
     return out
 
 

@@ -50,7 +50,7 @@ def _declared_functions():
 def test_header_declares_the_boundary():
     names = _declared_functions()
     for required in ("tdp_plan_create", "tdp_plan_info", "tdp_plan_destroy", "tdp_split",
-                     "tdp_norm_filter", "tdp_blend", "tdp_status_str"):
+                     "tdp_norm_filter", "tdp_split_filter", "tdp_blend", "tdp_status_str"):
         assert required in names
 
 
@@ -156,6 +156,21 @@ def test_host_validation_before_launch(tdp):
     assert lib.tdp_tile_mean(plan.handle, 3, 16, 16, None) == 4                                   # 12 bytes
     assert lib.tdp_tile_mean(plan.handle, 8, 16, 40, None) == 4
     assert lib.tdp_tile_mean(plan.handle, -1, 16, 16, None) == 1
+    # tdp_split_filter(plan, X, P, K, N, normalize, Y, Q, mn, mx, keep, idx, count, kcount, Kout, slot, s)
+    i32 = ctypes.c_int32
+    lib.tdp_split_filter.argtypes = [vp, vp, vp, vp, i32, i32] + [vp] * 11
+    ok = dict(X=16, P=8, K=8, N=4, Y=16, Q=8, mn=16, mx=16, keep=16, idx=16, count=16, kcount=16, Kout=16)
+
+    def sf(**kw):
+        a = dict(ok, **kw)
+        return lib.tdp_split_filter(plan.handle, a["X"], a["P"], a["K"], a["N"], 1, a["Y"], a["Q"], a["mn"],
+                                    a["mx"], a["keep"], a["idx"], a["count"], a["kcount"], a["Kout"],
+                                    a.get("slot"), None)
+    assert sf(P=None) == 1 and sf(Q=None) == 1                 # the bounds need positions
+    assert sf(N=-1) == 1
+    assert sf(mx=None) == 1 and sf(count=None) == 1 and sf(Kout=None) == 1
+    assert sf(X=24) == 4 and sf(K=12) == 4 and sf(slot=6) == 4 and sf(Q=4) == 4
+    assert lib.tdp_split_filter(None, 16, 8, 8, 4, 1, 16, 8, 16, 16, 16, 16, 16, 16, 16, None, None) == 1
 
 
 def test_binding_refuses_wrong_sizes_on_host(tdp):

@@ -1,4 +1,4 @@
-"""One TDP step (bounds, split, filter, blend) captured in a CUDA graph and replayed gives
+"""One TDP step (bounds, split, filter, blend; as separate calls or with tdp_split_filter) captured in a CUDA graph and replayed gives
 the same bytes as the same calls launched directly: the library allocates nothing and
 never synchronises, so its calls can sit inside a captured per-step graph."""
 import numpy as np
@@ -10,7 +10,8 @@ from gpu_path import to_dev
 pytestmark = pytest.mark.gpu
 
 
-def test_graph_replay_matches_direct_launches():
+@pytest.mark.parametrize("fused", [False, True])
+def test_graph_replay_matches_direct_launches(fused):
     import torch
 
     import __graft_entry__
@@ -31,9 +32,13 @@ def test_graph_replay_matches_direct_launches():
 
     def step(b, s):
         Y, Q, mn, mx, keep, idx, count, kcount, Kout, slot, Z = b
-        tdp.tdp_pos_bounds(plan, Pd, mn, mx, stream=s)
-        tdp.tdp_split(plan, Xd, Pd, mn, 1, Y, Q, stream=s)
-        tdp.tdp_norm_filter(plan, Kd, N, mn, mx, 1, keep, idx, count, kcount, Kout, slot, stream=s)
+        if fused:
+            tdp.tdp_split_filter(plan, Xd, Pd, Kd, N, 1, Y, Q, mn, mx, keep, idx, count, kcount, Kout, slot,
+                                 stream=s)
+        else:
+            tdp.tdp_pos_bounds(plan, Pd, mn, mx, stream=s)
+            tdp.tdp_split(plan, Xd, Pd, mn, 1, Y, Q, stream=s)
+            tdp.tdp_norm_filter(plan, Kd, N, mn, mx, 1, keep, idx, count, kcount, Kout, slot, stream=s)
         tdp.tdp_blend(plan, Yout, Z, stream=s)
 
     s = torch.cuda.Stream()

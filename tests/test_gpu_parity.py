@@ -38,18 +38,21 @@ def _yout(wl, Y, seed):
 
 
 def _check_path(tdp, wl, X, P, K, normalize=True, stream=None):
+    """Both forms of the pre-model stage (three calls, and tdp_split_filter) against the
+    oracle, bit for bit; then the blend."""
     plan = _plan(tdp, wl)
     p = oracle.problem_of(wl)
-    out = run_split_filter(tdp, plan, wl, X, P, K, normalize=normalize, stream=stream)
     Yref, Qref = oracle.split(p, X, P)
-    assert np.array_equal(out["Y"].reshape(Yref.shape), Yref), "tile split differs"
     mn, mx = oracle.bounds(p, Qref)
-    assert np.array_equal(out["mn"], mn) and np.array_equal(out["mx"], mx)
     Qn = oracle.normalize(p, Qref, mn) if normalize else Qref
-    assert np.array_equal(out["Q"], Qn), "tile positions differ"
     ref = dict(zip(("keep", "idx", "count", "kcount", "Kout", "slot"),
                    oracle.filter_cond(p, K, mn, mx, normalize, with_slot=True)))
-    assert_filter_equal(out, ref, plan.n_tiles, wl.B)
+    for fused in (False, True):
+        out = run_split_filter(tdp, plan, wl, X, P, K, normalize=normalize, stream=stream, fused=fused)
+        assert np.array_equal(out["Y"].reshape(Yref.shape), Yref), f"tile split differs (fused={fused})"
+        assert np.array_equal(out["mn"], mn) and np.array_equal(out["mx"], mx), f"bounds differ (fused={fused})"
+        assert np.array_equal(out["Q"], Qn), f"tile positions differ (fused={fused})"
+        assert_filter_equal(out, ref, plan.n_tiles, wl.B)
     # blend of noisy tile outputs
     Yout = _yout(wl, Yref, wl.seed + 99)
     Z = run_blend(tdp, plan, wl, Yout, stream=stream)
@@ -143,13 +146,16 @@ def test_parity_minimal_rows(tdp):
         _check_path(tdp, wl, X, P, K)
 
 
-def test_no_cond_tokens(tdp):
+@pytest.mark.parametrize("fused", [False, True])
+def test_no_cond_tokens(tdp, fused):
     wl = wk.by_name("small")
     X, P, _ = wk.make_inputs(wl)
     K = np.zeros((wl.B, 3, 0, 2), np.int32)
     plan = _plan(tdp, wl)
-    out = run_split_filter(tdp, plan, wl, X, P, K)
+    out = run_split_filter(tdp, plan, wl, X, P, K, fused=fused)
     assert (out["count"] == 0).all()
+    Yref, _ = oracle.split(oracle.problem_of(wl), X, P)
+    assert np.array_equal(out["Y"].reshape(Yref.shape), Yref)
 
 
 def test_split_without_positions(tdp):
@@ -170,21 +176,24 @@ def test_zero_batch(tdp):
     P = torch.empty((0, 3, wl.tokens, 2), dtype=torch.int32, device="cuda")
     tdp.tdp_pos_bounds(plan, P, mn, mx)
     tdp.tdp_split(plan, X, P, mn, 1, Y, Q)
+    K = torch.empty((0, 3, 4, 2), dtype=torch.int32, device="cuda")
+    keep, idx, count, kcount, Kout = tdp.alloc_filter_outputs(plan, 4, "cuda")
+    tdp.tdp_split_filter(plan, X, P, K, 4, 1, Y, Q, mn, mx, keep, idx, count, kcount, Kout)
     Z = torch.empty_like(X)
     tdp.tdp_blend(plan, Y, Z)
     torch.cuda.synchronize()
 
 
 def test_large_workload_in_bench_configuration(tdp):
-    """The large workload at full size, as the benchmark launches it: split and filter
-    compared in full, the blend on sampled cells (each computed alone by the oracle) and
-    through the reconstruction property over every element."""
+    """The large workload at full size, as the benchmark launches it (tdp_split_filter, then
+    tdp_blend): split and filter compared in full, the blend on sampled cells (each computed
+    alone by the oracle) and through the reconstruction property over every element."""
     import torch
     wl = wk.by_name("large")
     X, P, K = wk.make_inputs(wl)
     plan = _plan(tdp, wl)
     p = oracle.problem_of(wl)
-    out = run_split_filter(tdp, plan, wl, X, P, K)
+    out = run_split_filter(tdp, plan, wl, X, P, K, fused=True)
     Yref, Qref = oracle.split(p, X, P)
     assert np.array_equal(out["Y"].reshape(Yref.shape), Yref)
     mn, mx = oracle.bounds(p, Qref)
