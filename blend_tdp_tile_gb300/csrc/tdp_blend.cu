@@ -11,8 +11,10 @@
 // the per-vector work is table lookups, at most 8 independent 16-byte loads
 // issued back to back, fp32 FMAs in ascending tile order and one streaming
 // store.  Every tile-output byte is read exactly once and every latent byte
-// written once: no atomics, no scratch memory, no inter-block waits.  At most
-// 64 registers per thread keep 32 warps, and so enough loads, in flight per SM.
+// written once: no atomics, no scratch memory, no inter-block waits.  The
+// loads in flight bound a register-staged gather, so on rows with at most two
+// F/H combos (at most 4 loads per vector) a thread takes two vectors per pass,
+// with 80 registers and 24 warps per SM.
 #include "tdp.h"
 #include "tdp_device.cuh"
 #include "tdp_internal.h"
@@ -21,6 +23,8 @@ namespace {
 
 constexpr int kBlendThreads = 256;
 constexpr int kWTab = 1024;      // cells of the per-row W table built per pass
+constexpr int kBlendGroup = 2;   // output vectors per thread and pass on rows with <= 2 combos
+constexpr int kBlendMinBlocks = 3;   // blocks per SM the register budget is sized for
 
 // W-coverage of one cell: tiles iW0 (low 16 bits) and iW1 + 1 (high 16 bits,
 // 0 = none) and their ramp weights.
@@ -86,7 +90,7 @@ struct vec_math<1> {     // 8 x bf16
 };
 
 template <int BF16>
-__global__ void __launch_bounds__(kBlendThreads, 4)
+__global__ void __launch_bounds__(kBlendThreads, kBlendMinBlocks)
 tdp_blend_kernel(const __grid_constant__ tdp_geom g, int32_t cv_shift, const uint4 *__restrict__ Yout,
                  uint4 *__restrict__ Z)
 {
@@ -108,7 +112,9 @@ tdp_blend_kernel(const __grid_constant__ tdp_geom g, int32_t cv_shift, const uin
     const int32_t nW = g.d[2].n, oW = g.d[2].o;
     const int32_t CV = (g.C * g.esize) >> 4;
     const int64_t T = (int64_t)g.F * g.H * g.W;
-    uint4 *zrow = Z + ((int64_t)b * T + ((int64_t)f * g.H + h) * g.W) * CV;
+    // tile-row offsets in 16-byte vectors: cell w, vector cv of (combo c, W-tile iW)
+    // sits at Yout + s_tok[c * nW + iW] + w * CV + cv
+    for (int32_t e = threadIdx.x; e < rc.nc * nW; e += blockDim.x) s_tok[e] *= CV;
     const int32_t nc = rc.nc;
     float rFH[TDP_MAX_COMBOS];
 #pragma unroll
@@ -128,33 +134,74 @@ tdp_blend_kernel(const __grid_constant__ tdp_geom g, int32_t cv_shift, const uin
             s_w[i] = e;
         }
         __syncthreads();
+        // vector v of this pass is cell wbase + v / CV: at ybase + tile offset + v
+        const uint4 *ybase = Yout + (int64_t)wbase * CV;
+        uint4 *zbase = Z + ((int64_t)b * T + ((int64_t)f * g.H + h) * g.W + wbase) * CV;
         const int32_t nvec = wn * CV;
-        for (int32_t v = threadIdx.x; v < nvec; v += blockDim.x) {
-            const int32_t dw = cv_shift >= 0 ? (v >> cv_shift) : v / CV;
-            const int32_t cv = v - dw * CV;
-            const int32_t w = wbase + dw;
-            const tdp_wcell e = s_w[dw];
-            const int32_t iW0 = e.iw & 0xffff, iW1 = (e.iw >> 16) - 1;
-            // every load first (at most 8 in flight), then the arithmetic
-            uint4 y0[TDP_MAX_COMBOS], y1[TDP_MAX_COMBOS];
+        if (nc <= 2) {
+            // At most one F- or H-overlap on this row, so at most 4 loads per vector:
+            // kBlendGroup output vectors per thread and pass, all their loads in flight
+            // at once; each sum is formed in the same order as in the general loop.
+            constexpr int G = kBlendGroup;
+            for (int32_t v0 = threadIdx.x; v0 < nvec; v0 += G * blockDim.x) {
+                int32_t vq[G], iw[G];
+                uint4 y[G][2][2];                          // [vector][combo][W-tile]
 #pragma unroll
-            for (int c = 0; c < TDP_MAX_COMBOS; ++c) {
-                if (c < nc) {
-                    y0[c] = __ldcs(Yout + (s_tok[c * nW + iW0] + w) * CV + cv);
-                    if (iW1 >= 0) y1[c] = __ldcs(Yout + (s_tok[c * nW + iW1] + w) * CV + cv);
+                for (int q = 0; q < G; ++q) {
+                    const int32_t v = v0 + q * (int32_t)blockDim.x;
+                    vq[q] = v < nvec ? v : v0;             // past the end: repeat vector v0
+                    iw[q] = s_w[cv_shift >= 0 ? (vq[q] >> cv_shift) : vq[q] / CV].iw;
+                    const int32_t i0 = iw[q] & 0xffff, i1 = (iw[q] >> 16) - 1;
+                    if (v < nvec) {
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) {
+                            if (c < nc) {
+                                y[q][c][0] = __ldcs(ybase + s_tok[c * nW + i0] + vq[q]);
+                                if (i1 >= 0) y[q][c][1] = __ldcs(ybase + s_tok[c * nW + i1] + vq[q]);
+                            }
+                        }
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < G; ++q) {
+                    if (v0 + q * (int32_t)blockDim.x >= nvec) break;
+                    const tdp_wcell e = s_w[cv_shift >= 0 ? (vq[q] >> cv_shift) : vq[q] / CV];
+                    const bool two = (iw[q] >> 16) != 0;
+                    float acc[VM::kElems];
+                    VM::mul(acc, rFH[0] * e.r0, y[q][0][0]);
+                    if (two) VM::fma(acc, rFH[0] * e.r1, y[q][0][1]);
+                    if (nc > 1) {
+                        VM::fma(acc, rFH[1] * e.r0, y[q][1][0]);
+                        if (two) VM::fma(acc, rFH[1] * e.r1, y[q][1][1]);
+                    }
+                    __stcs(zbase + vq[q], VM::pack(acc));
                 }
             }
-            float acc[VM::kElems];
-            VM::mul(acc, rFH[0] * e.r0, y0[0]);          // the first term keeps the sign of zero
-            if (iW1 >= 0) VM::fma(acc, rFH[0] * e.r1, y1[0]);
+        } else {
+            for (int32_t v = threadIdx.x; v < nvec; v += blockDim.x) {
+                const tdp_wcell e = s_w[cv_shift >= 0 ? (v >> cv_shift) : v / CV];
+                const int32_t iW0 = e.iw & 0xffff, iW1 = (e.iw >> 16) - 1;
+                // every load first (at most 8 in flight), then the arithmetic
+                uint4 y0[TDP_MAX_COMBOS], y1[TDP_MAX_COMBOS];
 #pragma unroll
-            for (int c = 1; c < TDP_MAX_COMBOS; ++c) {
-                if (c < nc) {
-                    VM::fma(acc, rFH[c] * e.r0, y0[c]);
-                    if (iW1 >= 0) VM::fma(acc, rFH[c] * e.r1, y1[c]);
+                for (int c = 0; c < TDP_MAX_COMBOS; ++c) {
+                    if (c < nc) {
+                        y0[c] = __ldcs(ybase + s_tok[c * nW + iW0] + v);
+                        if (iW1 >= 0) y1[c] = __ldcs(ybase + s_tok[c * nW + iW1] + v);
+                    }
                 }
+                float acc[VM::kElems];
+                VM::mul(acc, rFH[0] * e.r0, y0[0]);          // the first term keeps the sign of zero
+                if (iW1 >= 0) VM::fma(acc, rFH[0] * e.r1, y1[0]);
+#pragma unroll
+                for (int c = 1; c < TDP_MAX_COMBOS; ++c) {
+                    if (c < nc) {
+                        VM::fma(acc, rFH[c] * e.r0, y0[c]);
+                        if (iW1 >= 0) VM::fma(acc, rFH[c] * e.r1, y1[c]);
+                    }
+                }
+                __stcs(zbase + v, VM::pack(acc));
             }
-            __stcs(zrow + (int64_t)w * CV + cv, VM::pack(acc));
         }
         __syncthreads();   // the table is rebuilt for the next cells
     }

@@ -145,10 +145,11 @@ __device__ __forceinline__ uint32_t tdp_pack_bf16x2(float lo, float hi)
 }
 
 // ---------------------------------------------------------------------------
-// Programmatic dependent launch.  Every kernel of the library lets the next
-// kernel in its stream launch early (tdp_pdl_trigger at its start) and waits
-// for the kernel before it to complete, with its memory visible, before it
-// touches global memory that kernel may write (tdp_pdl_wait).  The work before
+// Programmatic dependent launch.  The kernels of the library let the next
+// kernel in their stream launch early (tdp_pdl_trigger at their start; the two
+// latency-bound filter kernels instead let it launch as their blocks exit), and
+// every kernel waits for the kernel before it to complete, with its memory
+// visible, before it touches global memory that kernel may write (tdp_pdl_wait).  The work before
 // the wait is limited to kernel parameters and shared memory, except where a
 // kernel is launched only behind a kernel of this library whose own wait comes
 // first (stated at each such kernel).  Both are no-ops for a plain launch.

@@ -30,7 +30,9 @@ tdp_keep_kernel(const __grid_constant__ tdp_geom g, const int2 *__restrict__ K, 
                 int32_t *__restrict__ kcount)
 {
     __shared__ kcount_smem sm;
-    tdp_pdl_trigger();
+    // No early trigger here or in tdp_compact_kernel: the next kernel launches as these
+    // blocks exit.  Blocks of the next kernel waiting beside these latency-bound ones
+    // slowed them more than the early launch saved.
     tdp_pdl_wait();
     const int64_t nkeep = (int64_t)g.nt * g.B * nchunk;
     if ((int64_t)blockIdx.x < nkeep) {
@@ -82,7 +84,6 @@ tdp_compact_kernel(const __grid_constant__ tdp_geom g, const int2 *__restrict__ 
                    int32_t *__restrict__ slot)
 {
     __shared__ compact_smem sm;
-    tdp_pdl_trigger();
     tdp_pdl_wait();
     const int64_t tb = blockIdx.x / nchunk;
     const int32_t c = (int32_t)(blockIdx.x - tb * nchunk);
