@@ -23,6 +23,8 @@
 //        count blocks   wait, then the per-token count of keeping tiles.
 //      Filter and count blocks sit after the first split rows in block order, so
 //      they start once the bounds are done and run beside the HBM-bound copy.
+//      (Positions in blocks of their own, so that no split row waits, were slower:
+//      each such block rebuilt its row tables for little work.)
 #include <algorithm>
 #include <atomic>
 
@@ -44,30 +46,38 @@ struct split_smem {
     int32_t loW[TDP_MAX_TILES_PER_DIM], hiW[TDP_MAX_TILES_PER_DIM];
 };
 
-// One latent row (b, f, h) by one block.  CV = 16-byte vectors per token.
-// early: copy the latent before waiting on the previous kernel (see the file header).
-__device__ __forceinline__ void split_row(const tdp_geom &g, int32_t row, const uint4 *__restrict__ X,
-                                          const int2 *__restrict__ P, int32_t normalize, uint4 *__restrict__ Y,
-                                          int2 *__restrict__ Q, const int32_t *__restrict__ mn, bool early,
-                                          split_smem &sm)
+// The row table of latent row `row` = (b, f, h) in shared memory, with the
+// positions' part when `positions` is set.  Whole block; ends with a barrier.
+struct split_row_id {
+    int32_t b, f, h;
+    tdp_row_combos rc;
+};
+
+__device__ __forceinline__ split_row_id split_table(const tdp_geom &g, int32_t row, bool positions, split_smem &sm)
 {
-    const int32_t h = row % g.H, f = (row / g.H) % g.F, b = row / (g.H * g.F);
+    split_row_id r;
+    r.h = row % g.H;
+    r.f = (row / g.H) % g.F;
+    r.b = row / (g.H * g.F);
     for (int32_t i = threadIdx.x; i < g.d[2].n; i += blockDim.x) {
         sm.loW[i] = g.d[2].lo[i];
         sm.hiW[i] = g.d[2].hi[i];
     }
-    const tdp_row_combos rc = tdp_make_combos(g, f, h);
-    tdp_fill_row_table(g, rc, b, f, h, sm.tok, P ? sm.qpos : nullptr, P ? sm.Tt : nullptr,
-                       P ? sm.tb : nullptr);   // ends with a barrier
-    if (!early) tdp_pdl_wait();
-    const int32_t oW = g.d[2].o;
+    r.rc = tdp_make_combos(g, r.f, r.h);
+    tdp_fill_row_table(g, r.rc, r.b, r.f, r.h, sm.tok, positions ? sm.qpos : nullptr, positions ? sm.Tt : nullptr,
+                       positions ? sm.tb : nullptr);   // ends with a barrier
+    return r;
+}
 
-    const int32_t nW = g.d[2].n;
+// Latent of one row: every 16-byte vector is loaded once and stored to each tile
+// holding it.  CV = 16-byte vectors per token.
+__device__ __forceinline__ void split_latent(const tdp_geom &g, const split_row_id &r, const uint4 *__restrict__ X,
+                                             uint4 *__restrict__ Y, const split_smem &sm)
+{
+    const int32_t nW = g.d[2].n, oW = g.d[2].o;
     const int32_t CV = (g.C * g.esize) >> 4;
     const int64_t T = (int64_t)g.F * g.H * g.W;
-    const int64_t gtok = (int64_t)b * T + ((int64_t)f * g.H + h) * g.W;   // token of (b,f,h,0)
-
-    // latent: every 16-byte vector of the row is loaded once and stored to each tile
+    const int64_t gtok = (int64_t)r.b * T + ((int64_t)r.f * g.H + r.h) * g.W;   // token of (b,f,h,0)
     const int32_t nvec = g.W * CV;
     const uint4 *src = X + gtok * CV;
     for (int32_t v0 = threadIdx.x; v0 < nvec; v0 += kSplitUnroll * blockDim.x) {
@@ -83,21 +93,27 @@ __device__ __forceinline__ void split_row(const tdp_geom &g, int32_t row, const 
             if (v >= nvec) break;
             const int32_t w = v / CV, cv = v - w * CV;
             const tdp_cover cW = tdp_cover_tab(sm.loW, sm.hiW, nW, g.W, oW, w);
-            for (int32_t c = 0; c < rc.nc; ++c) {
+            for (int32_t c = 0; c < r.rc.nc; ++c) {
                 __stcs(Y + (sm.tok[c * nW + cW.i0] + w) * CV + cv, xs[u]);
                 if (cW.i1 >= 0) __stcs(Y + (sm.tok[c * nW + cW.i1] + w) * CV + cv, xs[u]);
             }
         }
     }
-    if (early) tdp_pdl_wait();                      // mn final from here on
-    if (!P) return;
+}
 
-    // positions: [B,3,T,2] -> tile-major [B,3,T_t,2], minus mn when normalising
+// Positions of one row: [B,3,T,2] -> tile-major [B,3,T_t,2], minus mn when normalising.
+__device__ __forceinline__ void split_positions(const tdp_geom &g, const split_row_id &r,
+                                                const int2 *__restrict__ P, int32_t normalize,
+                                                int2 *__restrict__ Q, const int32_t *__restrict__ mn,
+                                                const split_smem &sm)
+{
+    const int32_t nW = g.d[2].n, oW = g.d[2].o;
+    const int64_t T = (int64_t)g.F * g.H * g.W;
     for (int32_t q = threadIdx.x; q < 3 * g.W; q += blockDim.x) {
         const int32_t d = q / g.W, w = q - d * g.W;
-        const int2 p = __ldcs(P + ((int64_t)b * 3 + d) * T + ((int64_t)f * g.H + h) * g.W + w);
+        const int2 p = __ldcs(P + ((int64_t)r.b * 3 + d) * T + ((int64_t)r.f * g.H + r.h) * g.W + w);
         const tdp_cover cW = tdp_cover_tab(sm.loW, sm.hiW, nW, g.W, oW, w);
-        for (int32_t c = 0; c < rc.nc; ++c) {
+        for (int32_t c = 0; c < r.rc.nc; ++c) {
             for (int32_t k = 0; k < 2; ++k) {
                 const int32_t iW = k ? cW.i1 : cW.i0;
                 if (iW < 0) break;
@@ -114,7 +130,7 @@ __device__ __forceinline__ void split_row(const tdp_geom &g, int32_t row, const 
     }
 }
 
-// Block = one latent row (b, f, h).
+// Block = one latent row (b, f, h): latent and positions.
 __global__ void __launch_bounds__(kSplitThreads)
 tdp_split_kernel(const __grid_constant__ tdp_geom g, const uint4 *__restrict__ X,
                  const int2 *__restrict__ P, int32_t normalize, uint4 *__restrict__ Y,
@@ -122,12 +138,16 @@ tdp_split_kernel(const __grid_constant__ tdp_geom g, const uint4 *__restrict__ X
 {
     __shared__ split_smem sm;
     tdp_pdl_trigger();
-    split_row(g, blockIdx.x, X, P, normalize, Y, Q, mn, false, sm);
+    const split_row_id r = split_table(g, blockIdx.x, P != nullptr, sm);
+    tdp_pdl_wait();
+    split_latent(g, r, X, Y, sm);
+    if (P) split_positions(g, r, P, normalize, Q, mn, sm);
 }
 
 // Blocks [0, fpos): split rows 0..fpos-1; [fpos, fpos + nfilt): filter blocks
 // (tb = t*B + b); [fpos + nfilt, fpos + nfilt + ncount): count blocks; the rest:
-// split rows fpos.. .
+// split rows fpos.. .  Split rows copy their latent before waiting on the bounds
+// kernel (see the file header) and wait only for the normalised positions.
 __global__ void __launch_bounds__(kSplitThreads, 4)
 tdp_split_filter_kernel(const __grid_constant__ tdp_geom g, const uint4 *__restrict__ X,
                         const int2 *__restrict__ P, int32_t normalize, uint4 *__restrict__ Y,
@@ -153,8 +173,10 @@ tdp_split_filter_kernel(const __grid_constant__ tdp_geom g, const uint4 *__restr
             tdp_filt::kcount_block(g, K, N, mn, mx, kcount, r - nfilt, sm.kc);
         return;
     }
-    const int32_t row = blk < fpos ? blk : blk - nfilt - ncount;
-    split_row(g, row, X, P, normalize, Y, Q, mn, true, sm.split);
+    const split_row_id r = split_table(g, blk < fpos ? blk : blk - nfilt - ncount, true, sm.split);
+    split_latent(g, r, X, Y, sm.split);
+    tdp_pdl_wait();                                 // mn final from here on
+    split_positions(g, r, P, normalize, Q, mn, sm.split);
 }
 
 // Split blocks resident on the whole device at once (cached per device).
