@@ -404,6 +404,10 @@ def run_ours(args, rank, world, local_rank):
             Ou = torch.empty((wl.B, La), dtype=torch.bfloat16, device=dev)
         s.synchronize()
         extras = {}
+        # these inputs (~70 MB) fit in L2: each timed launch follows a read of 256 MB
+        # (which leaves no dirty lines), so it starts with its inputs in HBM
+        flush = torch.ones(256 << 20, dtype=torch.uint8, device=dev)
+        reps = 50
         for name, fn, nbytes in (
             ("cond_blend", lambda: tdp.tdp_cond_blend(plan, N, ncap, Yc, slot2, Oc, stream=s),
              kept_rows * wl.C * wl.esize + plan.n_tiles * wl.B * N * 4 + wl.B * N * wl.C * wl.esize),
@@ -411,14 +415,21 @@ def run_ours(args, rank, world, local_rank):
              (plan.n_tiles + 1) * wl.B * La * wl.esize)):
             for _ in range(5):
                 fn()
-            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a0.record(s)
-            for _ in range(100):
-                fn()
-            a1.record(s)
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+            with torch.cuda.stream(s):
+                # keep the GPU busy while the host queues every launch, so that no
+                # host-side gap falls between an event and its kernel
+                torch.cuda._sleep(int(3e7))
+                for a0, a1 in ev:
+                    flush.sum()
+                    a0.record(s)
+                    fn()
+                    a1.record(s)
             s.synchronize()
-            t_ms = a0.elapsed_time(a1) / 100
-            extras[name] = {"ms": t_ms, "algorithmic_bytes": nbytes, "GB/s": nbytes / (t_ms * 1e-3) / 1e9}
+            t_ms = statistics.mean(a0.elapsed_time(a1) for a0, a1 in ev)
+            extras[name] = {"ms": t_ms, "algorithmic_bytes": nbytes, "GB/s": nbytes / (t_ms * 1e-3) / 1e9,
+                            "frac": nbytes / (t_ms * 1e-3) / 1e9 / hbm_peak()[0],
+                            "timing": f"mean of {reps} launches, each after an L2 flush (256 MB read)"}
         extras["cond_blend"]["shape"] = f"{plan.n_tiles} tiles x {ncap} rows x {wl.C} ch, {kept_rows} kept rows"
         extras["tile_mean"]["shape"] = f"{plan.n_tiles} tiles x {AUDIO_TOKENS} audio tokens x {wl.C} ch (synthetic)"
 

@@ -20,13 +20,13 @@ static inline bool tdp_aligned(const void *p, uintptr_t a)
 
 #include <utility>
 
-// Launch `kernel` on stream `s`; with `pdl` set, as a programmatic dependent
-// launch: it may start once every block of the kernel before it in the stream
-// has run griddepcontrol.launch_dependents, and orders its own global-memory
-// work behind that kernel with griddepcontrol.wait.
+// Launch `kernel` on stream `s` with `smem` bytes of dynamic shared memory; with
+// `pdl` set, as a programmatic dependent launch: it may start once every block
+// of the kernel before it in the stream has run griddepcontrol.launch_dependents,
+// and orders its own global-memory work behind that kernel with griddepcontrol.wait.
 template <typename... KArgs, typename... Args>
-static inline cudaError_t tdp_launch(bool pdl, void (*kernel)(KArgs...), unsigned grid, unsigned block,
-                                     cudaStream_t s, Args &&...args)
+static inline cudaError_t tdp_launch_smem(bool pdl, void (*kernel)(KArgs...), unsigned grid, unsigned block,
+                                          size_t smem, cudaStream_t s, Args &&...args)
 {
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -34,11 +34,19 @@ static inline cudaError_t tdp_launch(bool pdl, void (*kernel)(KArgs...), unsigne
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(block);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// The same without dynamic shared memory.
+template <typename... KArgs, typename... Args>
+static inline cudaError_t tdp_launch(bool pdl, void (*kernel)(KArgs...), unsigned grid, unsigned block,
+                                     cudaStream_t s, Args &&...args)
+{
+    return tdp_launch_smem(pdl, kernel, grid, block, 0, s, std::forward<Args>(args)...);
 }
 
 // tdp_bounds_init_kernel (plain launch) then tdp_bounds_kernel (dependent launch)

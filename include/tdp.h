@@ -223,10 +223,11 @@ tdp_status tdp_split_filter(tdp_plan_t plan, const void *X, const int32_t *P, co
  *  blend weight 1/(number of tiles that kept it), so that it is not counted
  *  several times.)
  *
- * out[b,k,:] = (1/n) * sum over the tiles t that kept token k, ascending, of
- * Ycond[t,b,slot[t,b,k],:], n = number of those tiles; fp32 accumulation, one
- * division per element by n, stored in the plan's dtype.  A token that no tile
- * kept gets 0.
+ * out[b,k,:] = (1/n) * sum over the tiles t that kept token k of
+ * Ycond[t,b,slot[t,b,k],:], n = number of those tiles; fp32 accumulation in
+ * ascending t (for n > 16: sums of runs of 8 consecutive kept tiles, added in
+ * order), one division per element by n, stored in the plan's dtype.  A token
+ * that no tile kept gets 0.
  *
  *   N      conditioning tokens per batch item (>= 0).
  *   ncap   rows reserved per (tile, batch item) in Ycond (>= 1); slots >= ncap
@@ -246,8 +247,9 @@ tdp_status tdp_cond_blend(tdp_plan_t plan, int32_t N, int32_t ncap, const void *
  *  averaged across tiles; the page warns that this average is context for the
  *  video tiles, not a meaningful audio output.)
  *
- * out[b,l] = (sum over t of A[t,b,l]) / n_tiles, fp32 accumulation in ascending
- * t, stored in the plan's dtype.
+ * out[b,l] = (sum over t of A[t,b,l]) / n_tiles, fp32 accumulation: the tiles
+ * of each quarter of the tile range in ascending t, then the four quarters' sums
+ * in order; stored in the plan's dtype.
  *
  *   L    elements per batch item; L * sizeof(element) must be a multiple of 16.
  *   A    device [n_tiles, B, L] (plan dtype), read.

@@ -93,3 +93,23 @@ def test_cond_blend_many_tiles(tdp):
     wl = wk.by_name("tiny").replace(F=4, H=64, W=64, C=8, dtype="bf16", num_tiles=(2, 32, 32),
                                     overlap=(1, 2, 1), n_cond=300)
     _cond_case(tdp, wl)
+
+
+def test_cond_blend_ragged_tokens(tdp):
+    """Token counts that leave the last block of 32 tokens part-filled, two batch items."""
+    _cond_case(tdp, wk.by_name("small").replace(B=2, n_cond=1000))
+
+
+def test_cond_blend_wide_channels(tdp):
+    """4 KB rows (bf16 C=2048): 256 vectors per token, more than one pass of lanes."""
+    wl = wk.by_name("tiny").replace(F=2, H=6, W=10, C=2048, dtype="bf16", num_tiles=(1, 2, 2),
+                                    overlap=(0, 2, 2), n_cond=100)
+    _cond_case(tdp, wl)
+
+
+@pytest.mark.parametrize("nw", [16, 17])
+def test_cond_blend_tile_count_edges(tdp, nw):
+    """256 tiles (the largest count the staged kernel takes) and 272 (the warp-per-token kernel)."""
+    wl = wk.by_name("tiny").replace(F=2, H=48, W=52, C=8, dtype="bf16", num_tiles=(1, 16, nw),
+                                    overlap=(0, 1, 1), n_cond=200)
+    _cond_case(tdp, wl)
