@@ -29,7 +29,6 @@
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kTileUnroll = 16;   // tiles whose loads a thread keeps in flight
 constexpr int kMeanVecs = 64;     // output vectors per tile-mean block
 constexpr int kMeanParts = 4;     // threads per output vector, each over a quarter of the tiles
 constexpr int kMeanUnroll = 8;    // tile loads a tile-mean thread keeps in flight
