@@ -75,13 +75,25 @@ def algorithmic_bytes(wl, total_tile_tokens, n_tiles, kept_total=None):
     return dict(bounds=bounds, split=split, filter=filt, blend=blend, step=mnmx + split + filt + blend)
 
 
-def config_of(wl, plan_tokens, n_tiles, parallelism):
+L2_BYTES = 129 << 20          # GB300 L2
+
+
+def config_of(wl, plan_tokens, n_tiles, parallelism, device=True):
+    tile_bytes = wl.B * plan_tokens * wl.C * wl.esize
+    lat_bytes = wl.latent_bytes()
+    sizes = f"tile outputs {tile_bytes / 1e9:.2f} GB, latent {lat_bytes / 1e9:.2f} GB per step"
+    if not device:
+        l2 = f"host CPU ({sizes})"
+    elif tile_bytes > L2_BYTES:
+        l2 = f"inputs larger than L2 ({sizes}); no flush"
+    else:
+        l2 = f"inputs fit in L2 ({sizes}): not an HBM measurement"
     return {
         "workload": (f"{wl.name}: B={wl.B} F={wl.F} H={wl.H} W={wl.W} C={wl.C} {wl.dtype}, "
                      f"tiles {'x'.join(map(str, wl.num_tiles))}, overlap {tuple(wl.overlap)}, "
                      f"{n_tiles} tiles / {plan_tokens} tile tokens, {wl.n_cond} cond tokens"),
         "parallelism": parallelism,
-        "l2": "inputs larger than L2 (tile outputs 1.27 GB, latent 0.40 GB per step); no flush",
+        "l2": l2,
     }
 
 
@@ -572,7 +584,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_of(wl_full, int(off_full[-1]), box_full.shape[0], "host CPU, 1 thread"),
+        "config": config_of(wl_full, int(off_full[-1]), box_full.shape[0], "host CPU, 1 thread", device=False),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
