@@ -13,8 +13,8 @@
 // store.  Every tile-output byte is read exactly once and every latent byte
 // written once: no atomics, no scratch memory, no inter-block waits.  The
 // loads in flight bound a register-staged gather, so on rows with at most two
-// F/H combos (at most 4 loads per vector) a thread takes two vectors per pass,
-// with 80 registers and 24 warps per SM.
+// F/H combos a thread takes four (one combo) or two (two combos) vectors per
+// pass, up to 8 loads in flight, with 80 registers and 24 warps per SM.
 #include "tdp.h"
 #include "tdp_device.cuh"
 #include "tdp_internal.h"
@@ -23,7 +23,6 @@ namespace {
 
 constexpr int kBlendThreads = 256;
 constexpr int kWTab = 1024;      // cells of the per-row W table built per pass
-constexpr int kBlendGroup = 2;   // output vectors per thread and pass on rows with <= 2 combos
 constexpr int kBlendMinBlocks = 3;   // blocks per SM the register budget is sized for
 
 // W-coverage of one cell: tiles iW0 (low 16 bits) and iW1 + 1 (high 16 bits,
@@ -139,42 +138,51 @@ tdp_blend_kernel(const __grid_constant__ tdp_geom g, int32_t cv_shift, const uin
         uint4 *zbase = Z + ((int64_t)b * T + ((int64_t)f * g.H + h) * g.W + wbase) * CV;
         const int32_t nvec = wn * CV;
         if (nc <= 2) {
-            // At most one F- or H-overlap on this row, so at most 4 loads per vector:
-            // kBlendGroup output vectors per thread and pass, all their loads in flight
-            // at once; each sum is formed in the same order as in the general loop.
-            constexpr int G = kBlendGroup;
-            for (int32_t v0 = threadIdx.x; v0 < nvec; v0 += G * blockDim.x) {
-                int32_t vq[G], iw[G];
-                uint4 y[G][2][2];                          // [vector][combo][W-tile]
+            // At most one F- or H-overlap on this row: four load slots of two W-tiles
+            // each.  One combo: slot s is vector s (4 vectors per pass); two combos:
+            // slot s is combo s & 1 of vector s >> 1 (2 vectors per pass).  Every load
+            // of the pass is in flight before any arithmetic; each sum is formed in the
+            // same order as in the general loop.
+            const int32_t vpp = nc == 1 ? 4 : 2;           // vectors per pass (block-uniform)
+            for (int32_t v0 = threadIdx.x; v0 < nvec; v0 += vpp * (int32_t)blockDim.x) {
+                int32_t vq[4], iw[4];
+                uint4 y[4][2];                             // [slot][W-tile]
 #pragma unroll
-                for (int q = 0; q < G; ++q) {
-                    const int32_t v = v0 + q * (int32_t)blockDim.x;
-                    vq[q] = v < nvec ? v : v0;             // past the end: repeat vector v0
-                    iw[q] = s_w[cv_shift >= 0 ? (vq[q] >> cv_shift) : vq[q] / CV].iw;
-                    const int32_t i0 = iw[q] & 0xffff, i1 = (iw[q] >> 16) - 1;
+                for (int sl = 0; sl < 4; ++sl) {
+                    const int32_t qv = nc == 1 ? sl : sl >> 1, c = nc == 1 ? 0 : sl & 1;
+                    const int32_t v = v0 + qv * (int32_t)blockDim.x;
+                    vq[sl] = v < nvec ? v : v0;            // past the end: repeat vector v0
+                    iw[sl] = s_w[cv_shift >= 0 ? (vq[sl] >> cv_shift) : vq[sl] / CV].iw;
+                    const int32_t i0 = iw[sl] & 0xffff, i1 = (iw[sl] >> 16) - 1;
                     if (v < nvec) {
-#pragma unroll
-                        for (int c = 0; c < 2; ++c) {
-                            if (c < nc) {
-                                y[q][c][0] = __ldcs(ybase + s_tok[c * nW + i0] + vq[q]);
-                                if (i1 >= 0) y[q][c][1] = __ldcs(ybase + s_tok[c * nW + i1] + vq[q]);
-                            }
-                        }
+                        y[sl][0] = __ldcs(ybase + s_tok[c * nW + i0] + vq[sl]);
+                        if (i1 >= 0) y[sl][1] = __ldcs(ybase + s_tok[c * nW + i1] + vq[sl]);
                     }
                 }
+                if (nc == 1) {
 #pragma unroll
-                for (int q = 0; q < G; ++q) {
-                    if (v0 + q * (int32_t)blockDim.x >= nvec) break;
-                    const tdp_wcell e = s_w[cv_shift >= 0 ? (vq[q] >> cv_shift) : vq[q] / CV];
-                    const bool two = (iw[q] >> 16) != 0;
-                    float acc[VM::kElems];
-                    VM::mul(acc, rFH[0] * e.r0, y[q][0][0]);
-                    if (two) VM::fma(acc, rFH[0] * e.r1, y[q][0][1]);
-                    if (nc > 1) {
-                        VM::fma(acc, rFH[1] * e.r0, y[q][1][0]);
-                        if (two) VM::fma(acc, rFH[1] * e.r1, y[q][1][1]);
+                    for (int q = 0; q < 4; ++q) {
+                        if (v0 + q * (int32_t)blockDim.x >= nvec) break;
+                        const tdp_wcell e = s_w[cv_shift >= 0 ? (vq[q] >> cv_shift) : vq[q] / CV];
+                        float acc[VM::kElems];
+                        VM::mul(acc, rFH[0] * e.r0, y[q][0]);
+                        if ((iw[q] >> 16) != 0) VM::fma(acc, rFH[0] * e.r1, y[q][1]);
+                        __stcs(zbase + vq[q], VM::pack(acc));
                     }
-                    __stcs(zbase + vq[q], VM::pack(acc));
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        if (v0 + q * (int32_t)blockDim.x >= nvec) break;
+                        const int32_t sl = 2 * q;
+                        const tdp_wcell e = s_w[cv_shift >= 0 ? (vq[sl] >> cv_shift) : vq[sl] / CV];
+                        const bool two = (iw[sl] >> 16) != 0;
+                        float acc[VM::kElems];
+                        VM::mul(acc, rFH[0] * e.r0, y[sl][0]);
+                        if (two) VM::fma(acc, rFH[0] * e.r1, y[sl][1]);
+                        VM::fma(acc, rFH[1] * e.r0, y[sl + 1][0]);
+                        if (two) VM::fma(acc, rFH[1] * e.r1, y[sl + 1][1]);
+                        __stcs(zbase + vq[sl], VM::pack(acc));
+                    }
                 }
             }
         } else {
