@@ -39,6 +39,11 @@
  *     failure returns TDP_ERR_CUDA; tdp_last_error_detail() then holds the
  *     CUDA error string.  Faults inside a kernel surface on the stream's next
  *     synchronisation, as for any CUDA work.  No C++ exception crosses the ABI.
+ *   - Kernels use programmatic dependent launch: a kernel may begin while the
+ *     kernel before it in the stream finishes, and waits for that kernel to
+ *     complete before it touches memory the kernel may write.  To the caller,
+ *     stream order is that of plain launches: a call's results are visible to
+ *     whatever is queued after it.
  *   - A plan is immutable once created and may be used concurrently from any
  *     number of host threads and streams.
  *   - Position arithmetic is int32 and wraps modulo 2^32.
