@@ -502,11 +502,31 @@ def run_ours(args, rank, world, local_rank):
         e1.record(s_in)
         torch.cuda.synchronize()
         e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+        # the same copies without the kernels, on the same two streams: the host
+        # link's floor for this leg on this machine (reported, not subtracted)
+        torch.cuda.synchronize()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(s_in)
+        s_out.wait_event(f0)
+        for i in range(args.e2e_steps):
+            j = i % 2
+            with torch.cuda.stream(s_in):
+                Xb[j].view(torch.int16).copy_(Xh, non_blocking=True)
+                Pb[j].copy_(Ph, non_blocking=True)
+                Kb[j].copy_(Kh, non_blocking=True)
+            with torch.cuda.stream(s_out):
+                Zh[j].copy_(Zb[j].view(torch.int16), non_blocking=True)
+        s_in.wait_stream(s_out)
+        f1.record(s_in)
+        torch.cuda.synchronize()
+        floor_ms = f0.elapsed_time(f1) / args.e2e_steps
         if world > 1:
             e2e_ms = max_over_ranks(e2e_ms, dev)
+        h2d, d2h = X.nbytes + P.nbytes + K.nbytes, X.nbytes
         e2e = {"value": world * ab["step"] / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
-               "h2d_bytes_per_step": X.nbytes + P.nbytes + K.nbytes, "d2h_bytes_per_step": X.nbytes,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_ms, "steps": args.e2e_steps,
+               "copy_floor_ms_per_step": floor_ms, "copy_floor_GBps": (h2d + d2h) / (floor_ms * 1e-3) / 1e9,
                "pipelining": "copies of steps i+1 (in) and i-1 (out) overlap step i on separate streams"}
 
     if rank != 0:
