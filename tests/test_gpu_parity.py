@@ -122,6 +122,8 @@ def test_parity_wrapping_positions(tdp):
     dict(num_tiles=(2, 2, 2), overlap=(1, 1, 1)),              # odd overlap of one cell
     dict(num_tiles=(3, 2, 3), overlap=(3, 5, 3)),              # odd overlaps, uneven cores
     dict(H=32, W=40, num_tiles=(1, 2, 2), overlap=(0, 16, 20)),  # overlap == core: overlaps touch
+    dict(F=3, H=8, W=12, num_tiles=(3, 8, 12), overlap=(1, 1, 0)),  # a tile per cell: one-cell cores
+    dict(F=4, H=10, W=9, num_tiles=(2, 5, 3), overlap=(2, 2, 3)),   # overlap == core in every dimension
 ])
 def test_parity_geometries(tdp, shape):
     base = wk.by_name("temporal").replace(F=9, H=26, W=30, C=24, n_cond=500)
