@@ -84,3 +84,21 @@ def test_committed_traffic_file_parses():
     for parts in lines:
         assert parts[0] in bench.KERNEL_SOURCES and len(parts[1]) == 16
         assert all(np.int64(int(x)) >= 0 for x in parts[2:6])
+
+
+def test_reference_arm_under_torchrun_prints_one_line():
+    """Launched as the driver launches N > 1 (torchrun, one process per rank): rank 0 alone
+    runs the oracle and prints; the other ranks exit 0 without work."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+                        "--master-addr", "127.0.0.1", "--master-port", str(port),
+                        os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2", "--workload", "tiny",
+                        "--steps", "1", "--warmup", "3"],
+                       capture_output=True, text=True, timeout=900, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip().startswith("{")]
+    assert len(lines) == 1, r.stdout[-2000:]
+    assert json.loads(lines[0])["impl"] == "reference"
