@@ -14,16 +14,17 @@
 // written once: no atomics, no scratch memory, no inter-block waits.  The
 // loads in flight bound a register-staged gather, so on rows with at most two
 // F/H combos a thread takes four (one combo) or two (two combos) vectors per
-// pass, up to 8 loads in flight, with 80 registers and 24 warps per SM.
+// pass, up to 8 loads in flight, with 80 registers and 24 warps per SM (six
+// 128-thread blocks, so that more rows are in flight at once).
 #include "tdp.h"
 #include "tdp_device.cuh"
 #include "tdp_internal.h"
 
 namespace {
 
-constexpr int kBlendThreads = 256;
+constexpr int kBlendThreads = 128;
 constexpr int kWTab = 1024;      // cells of the per-row W table built per pass
-constexpr int kBlendMinBlocks = 3;   // blocks per SM the register budget is sized for
+constexpr int kBlendMinBlocks = 6;   // blocks per SM the register budget is sized for
 
 // W-coverage of one cell: tiles iW0 (low 16 bits) and iW1 + 1 (high 16 bits,
 // 0 = none) and their ramp weights.
