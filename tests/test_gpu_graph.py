@@ -69,3 +69,48 @@ def test_graph_replay_matches_direct_launches(fused):
             continue
         assert torch.equal(a.view(torch.uint8) if a.dtype == torch.bfloat16 else a,
                            b.view(torch.uint8) if b.dtype == torch.bfloat16 else b), name
+
+
+def test_first_call_inside_graph_capture():
+    """A fresh process whose first tdp_split_filter call is made while a CUDA graph is being
+    captured (so nothing the library computes once per device is cached yet): the capture
+    succeeds and its replay matches direct launches."""
+    import subprocess
+    import sys
+    code = r'''
+import sys, numpy as np, torch
+sys.path.insert(0, ".")
+import __graft_entry__; __graft_entry__.build()
+import blend_tdp_tile_gb300 as tdp
+import workloads as wk
+sys.path.insert(0, "tests")
+from gpu_path import to_dev
+wl = wk.by_name("small")
+X, P, K = wk.make_inputs(wl)
+plan = tdp.tdp_plan_create(wl.B, wl.F, wl.H, wl.W, wl.C, wl.dtype, wl.num_tiles, wl.overlap)
+N = K.shape[2]
+Xd, Pd, Kd = to_dev(X), to_dev(P), to_dev(K)
+def bufs():
+    Y, Q, mn, mx = tdp.alloc_split_outputs(plan, "cuda")
+    return [Y, Q, mn, mx, *tdp.alloc_filter_outputs(plan, N, "cuda")]
+def call(b, s):
+    Y, Q, mn, mx, keep, idx, count, kcount, Kout = b
+    tdp.tdp_split_filter(plan, Xd, Pd, Kd, N, 1, Y, Q, mn, mx, keep, idx, count, kcount, Kout, stream=s)
+s = torch.cuda.Stream()
+graphed, direct = bufs(), bufs()
+torch.cuda.synchronize()
+g = torch.cuda.CUDAGraph()
+with torch.cuda.graph(g, stream=s):
+    call(graphed, s)
+g.replay()
+with torch.cuda.stream(s):
+    call(direct, s)
+torch.cuda.synchronize()
+for a, b in zip(direct[:4] + direct[4:8], graphed[:4] + graphed[4:8]):
+    assert torch.equal(a.view(torch.uint8) if a.dtype == torch.bfloat16 else a,
+                       b.view(torch.uint8) if b.dtype == torch.bfloat16 else b)
+print("ok")
+'''
+    root = __import__("os").path.dirname(__import__("os").path.dirname(__import__("os").path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=600, cwd=root)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), (r.stdout[-2000:], r.stderr[-3000:])
