@@ -48,7 +48,7 @@ LAUNCHES_PER_STEP = {
     "fused": 4,       # bounds init, bounds, split + filter, blend
     "separate": 6,    # bounds init, bounds, split, keep, compact, blend
 }
-PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.txt")
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "dram_traffic_large.txt")
 INSTRUMENT_EVERY = 10        # steps between those timed call by call
 
 

@@ -62,7 +62,7 @@ def test_traffic_file_parser(tmp_path, monkeypatch):
     rows = {k: bench.kernel_source_hash(v) for k, v in bench.KERNEL_SOURCES.items()}
     text = "# comment line\n" + "\n".join(
         f"{k} {h} {100 + i} {10 + i} 5 0" for i, (k, h) in enumerate(sorted(rows.items()))) + "\n"
-    f = tmp_path / "traffic.txt"
+    f = tmp_path / "dram_traffic_large.txt"
     f.write_text(text)
     monkeypatch.setattr(bench, "PROFILE_TRAFFIC", str(f))
     order = sorted(rows)
