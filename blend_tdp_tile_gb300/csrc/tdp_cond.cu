@@ -1,27 +1,30 @@
 // tdp_cond.cu -- the two reductions over tiles besides the latent blend
 // ("Tiled Data Parallelism (TDP)"):
-//   tdp_cond_blend_kernel  each conditioning token's per-tile outputs averaged
+//   tdp_cond_blend_runs_kernel, tdp_cond_blend_kernel
+//                          each conditioning token's per-tile outputs averaged
 //                          over the tiles that kept it ("Shared negative
 //                          (reference) positions": weight 1/(tiles that kept it));
 //   tdp_tile_mean_kernel   the audio latent averaged over all tiles ("What it
 //                          is": audio is processed on every tile and averaged).
 // Both are gather form and accumulate in fp32; no atomics, no scratch.  The
-// conditioning blend adds each token's rows in ascending tile order (in runs of
-// kListRows rows whose sums are added in order, for a token kept by many tiles);
-// the tile mean adds the tiles of each quarter of the tile range in ascending
-// order and then the four quarters' sums in order.
+// conditioning blend sums each token's rows in ascending tile order in runs of
+// kRunRows rows and adds the runs' sums in order; the tile mean adds the tiles of
+// each quarter of the tile range in ascending order and then the four quarters'
+// sums in order.
 //
 // tdp_cond_blend has two kernels.  With at most kStageTiles tiles (and rows of
-// Ycond numbered below 2^32), a block takes kBlockTok consecutive tokens of one
-// batch item: it stages their slots [tile][token] in shared memory (each tile's
-// slots are one coalesced read) and lists per token, in ascending tile order,
-// the rows of Ycond of the tiles that kept it.  A token kept by at most kLightRows tiles gets a group of lanes
-// across its channel vectors that sums its rows one by one, kListRows loads
-// in flight.  A token kept by more (a negative-time token is kept by every
-// tile) gets the whole block: each group sums a run of kListRows consecutive
-// rows of its list, and the runs' sums are added in order, so one such token
-// does not hold its block for many rounds of loads.  With more than
-// kStageTiles tiles, a warp per token reads the slots of 32 tiles at a time.
+// Ycond numbered below 2^32), tdp_cond_blend_runs_kernel gives a block kRunTok
+// consecutive tokens of one batch item: it stages their slots [tile][token] in
+// shared memory (each tile's slots are one coalesced read), lists per token, in
+// ascending tile order, the rows of Ycond of the tiles that kept it, and cuts
+// every list into runs of kRunRows rows.  The block's runs, token after token,
+// are dealt to its lane groups (lanes across a token's channel vectors), which
+// sum them one after another with no barrier in between, so a token kept by
+// every tile (a negative-time token) is spread over all groups.  A token with
+// one run is written by the group that summed it; the run sums of a token with
+// more wait in shared memory and are added in order once per chunk of runs.
+// With more than kStageTiles tiles, tdp_cond_blend_kernel gives each token a
+// warp, which reads the token's slots 32 tiles at a time.
 #include "tdp.h"
 #include "tdp_device.cuh"
 #include "tdp_internal.h"
@@ -32,10 +35,12 @@ constexpr int kThreads = 256;
 constexpr int kMeanVecs = 64;     // output vectors per tile-mean block
 constexpr int kMeanParts = 4;     // threads per output vector, each over a quarter of the tiles
 constexpr int kMeanUnroll = 8;    // tile loads a tile-mean thread keeps in flight
-constexpr int kStageTiles = 256;  // tiles the staged conditioning blend handles
-constexpr int kBlockTok = 16;     // tokens per block of the staged conditioning blend
-constexpr int kListRows = 8;      // row loads in flight per lane in the staged conditioning blend
-constexpr int kLightRows = 16;    // kept tiles up to which a token is summed by one lane group
+constexpr int kStageTiles = 256;  // tiles the run kernel of the conditioning blend handles
+constexpr int kRunThreads = 128;  // threads per block of the run kernel
+constexpr int kRunTok = 8;        // tokens per block of the run kernel (at most 32)
+constexpr int kRunMinBlocks = 8;  // resident blocks per SM the run kernel is compiled for
+constexpr int kRunRows = 8;       // rows per run: a token's kept rows are summed in runs of 8
+constexpr int kPartFloats = 4096; // shared-memory floats for the run sums of a chunk of runs
 
 template <int BF16>
 __device__ __forceinline__ void acc_add(float (&a)[8], const uint4 &y)
@@ -68,7 +73,8 @@ __device__ __forceinline__ uint4 acc_div(const float (&a)[8], float n)
 // Warp = one conditioning token (b, k).  Per round of 32 tiles, lane l loads the
 // token's slot in tile t0 + l; a ballot gives the tiles that kept it, in
 // ascending order, and their rows (lanes across the channel vectors) are loaded
-// up to kRowsInFlight at a time and accumulated in that order.
+// up to kRowsInFlight at a time and summed in that order in runs of kRunRows,
+// each run's sum added to the total when it is complete.
 constexpr int kRowsInFlight = 4;
 
 template <int BF16>
@@ -85,7 +91,8 @@ tdp_cond_blend_kernel(const __grid_constant__ tdp_geom g, int32_t N, int32_t nca
     for (int32_t cv0 = 0; cv0 < CV; cv0 += 32) {
         const int32_t cv = cv0 + lane;
         const bool act = cv < CV;
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // runs before the current one
+        float run[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // the current run of kRunRows rows
         int32_t n = 0;
         for (int32_t t0 = 0; t0 < g.nt; t0 += 32) {
             const int32_t t = t0 + lane;
@@ -106,122 +113,190 @@ tdp_cond_blend_kernel(const __grid_constant__ tdp_geom g, int32_t N, int32_t nca
                     }
                 }
 #pragma unroll
-                for (int u = 0; u < kRowsInFlight; ++u)
-                    if (u < got && act) acc_add<BF16>(acc, y[u]);
+                for (int u = 0; u < kRowsInFlight; ++u) {
+                    if (u < got && act) acc_add<BF16>(run, y[u]);
+                    if (u < got && (n + u + 1) % kRunRows == 0) {       // a run is complete
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            acc[e] += run[e];
+                            run[e] = 0.f;
+                        }
+                    }
+                }
                 n += got;
             }
+        }
+        if (n % kRunRows != 0) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] += run[e];
         }
         if (act) __stcs(out + tok * CV + cv, n > 0 ? acc_div<BF16>(acc, (float)n) : make_uint4(0u, 0u, 0u, 0u));
     }
 }
 
-struct cond_smem {
-    int32_t slot[kStageTiles][kBlockTok + 1];      // +1: column reads spread over the banks
-    uint32_t row[kBlockTok][kStageTiles];          // kept rows of Ycond per token, ascending tile
-    int32_t len[kBlockTok];
-    float part[8][kThreads];                       // run sums of a heavy token, one per lane
-};
+// Shared memory of the run kernel for nt tiles (dynamic; offsets in bytes):
+//   row   [kRunTok][nt]  uint32  kept rows of Ycond per token, ascending tile
+//   slot  [nt][kRunTok + 1] int32  staged slots (+1: column reads spread over the banks),
+//         reused after the lists are built as part [8][P][lpt] float: run sums of a chunk
+//         of P = kPartFloats / (8 lpt) runs
+//   carry [2][8][32] float  sum so far of the token that continues past a chunk (by chunk parity)
+//   len   [kRunTok] int32, run0 [kRunTok + 1] int32  (first run of each token; run0[kRunTok] = runs)
+//   tab   [kRunTok * ceil(nt / kRunRows)] uint16  run -> (token << 8) | run index within the token
+__host__ __device__ constexpr size_t run_max(size_t a, size_t b) { return a > b ? a : b; }
 
-// Sum rows i0 .. i0 + kListRows - 1 (those below len) of token j's list into acc.
+struct run_layout {
+    size_t slot, carry, len, run0, tab, bytes;
+    __host__ __device__ constexpr explicit run_layout(int32_t nt)
+        : slot((size_t)kRunTok * nt * 4),
+          carry(slot + run_max((size_t)nt * (kRunTok + 1) * 4, (size_t)kPartFloats * 4)),
+          len(carry + 2 * 8 * 32 * 4),
+          run0(len + kRunTok * 4),
+          tab(run0 + (kRunTok + 1) * 4),
+          bytes((tab + (size_t)kRunTok * ((nt + kRunRows - 1) / kRunRows) * 2 + 15) & ~(size_t)15)
+    {
+    }
+};
+static_assert(run_layout(kStageTiles).bytes <= 48 * 1024, "run kernel shared memory must fit the default 48 KB");
+
+// Sum rows i0 .. i0 + kRunRows - 1 (those below len) of a token's list into acc, in order.
 template <int BF16>
-__device__ __forceinline__ void cond_rows(const cond_smem &sm, const uint4 *__restrict__ Ycond, int32_t CV,
-                                          int32_t cv, int32_t j, int32_t i0, int32_t len, float (&acc)[8])
+__device__ __forceinline__ void run_rows(const uint32_t *rows, const uint4 *__restrict__ Ycond, int32_t CV,
+                                         int32_t cv, int32_t i0, int32_t len, float (&acc)[8])
 {
-    uint4 y[kListRows];
+    uint4 y[kRunRows];
 #pragma unroll
-    for (int u = 0; u < kListRows; ++u)
-        if (i0 + u < len) y[u] = __ldcs(Ycond + (int64_t)sm.row[j][i0 + u] * CV + cv);
+    for (int u = 0; u < kRunRows; ++u)
+        if (i0 + u < len) y[u] = __ldcs(Ycond + (int64_t)rows[i0 + u] * CV + cv);
 #pragma unroll
-    for (int u = 0; u < kListRows; ++u)
+    for (int u = 0; u < kRunRows; ++u)
         if (i0 + u < len) acc_add<BF16>(acc, y[u]);
 }
 
-// Block = tokens k0 .. k0 + kBlockTok - 1 of batch item b.
+// Block = tokens k0 .. k0 + kRunTok - 1 of batch item b.
 template <int BF16>
-__global__ void __launch_bounds__(kThreads, 3)
-tdp_cond_blend_staged_kernel(const __grid_constant__ tdp_geom g, int32_t N, int32_t ncap, int32_t CV, int32_t lpt,
-                             const uint4 *__restrict__ Ycond, const int32_t *__restrict__ slot,
-                             uint4 *__restrict__ out)
+__global__ void __launch_bounds__(kRunThreads, kRunMinBlocks)
+tdp_cond_blend_runs_kernel(const __grid_constant__ tdp_geom g, int32_t N, int32_t ncap, int32_t CV, int32_t lpt,
+                           const uint4 *__restrict__ Ycond, const int32_t *__restrict__ slot,
+                           uint4 *__restrict__ out)
 {
-    __shared__ cond_smem sm;
+    extern __shared__ __align__(16) unsigned char dsm[];
+    const int32_t nt = g.nt;
+    const run_layout L(nt);
+    uint32_t *s_row = reinterpret_cast<uint32_t *>(dsm);
+    int32_t *s_slot = reinterpret_cast<int32_t *>(dsm + L.slot);
+    float *s_part = reinterpret_cast<float *>(dsm + L.slot);
+    float *s_carry = reinterpret_cast<float *>(dsm + L.carry);
+    int32_t *s_len = reinterpret_cast<int32_t *>(dsm + L.len);
+    int32_t *s_run0 = reinterpret_cast<int32_t *>(dsm + L.run0);
+    uint16_t *s_tab = reinterpret_cast<uint16_t *>(dsm + L.tab);
     tdp_pdl_trigger();
     tdp_pdl_wait();
-    const int32_t nkb = (N + kBlockTok - 1) / kBlockTok;
-    const int32_t b = blockIdx.x / nkb, k0 = (blockIdx.x - b * nkb) * kBlockTok;
+    const int32_t nkb = (N + kRunTok - 1) / kRunTok;
+    const int32_t b = blockIdx.x / nkb, k0 = (blockIdx.x - b * nkb) * kRunTok;
     const int32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int32_t nt = g.nt;
-    // slots of the block's tokens in every tile, all of a thread's loads in flight
-    // before any is stored
+    // slots of the block's tokens in every tile (each tile's are one coalesced read),
+    // all of a thread's loads in flight before any is stored
     {
-        constexpr int kPer = kStageTiles * kBlockTok / kThreads;   // loads per thread
-        constexpr int kStep = kThreads / kBlockTok;                 // tiles per pass of the block
-        const int32_t j = threadIdx.x % kBlockTok;
+        constexpr int kStep = kRunThreads / kRunTok;               // tiles per pass of the block
+        constexpr int kPer = kStageTiles / kStep;                  // loads per thread
+        const int32_t j = threadIdx.x % kRunTok, t0 = threadIdx.x / kRunTok;
         const bool tok_ok = k0 + j < N;
-        const int32_t tb0 = threadIdx.x / kBlockTok;
         int32_t v[kPer];
 #pragma unroll
         for (int u = 0; u < kPer; ++u) {
-            const int32_t t = tb0 + u * kStep;
+            const int32_t t = t0 + u * kStep;
             v[u] = t < nt && tok_ok ? __ldg(slot + ((int64_t)t * g.B + b) * N + k0 + j) : -1;
         }
 #pragma unroll
         for (int u = 0; u < kPer; ++u) {
-            const int32_t t = tb0 + u * kStep;
-            if (t < nt) sm.slot[t][j] = v[u];
+            const int32_t t = t0 + u * kStep;
+            if (t < nt) s_slot[t * (kRunTok + 1) + j] = v[u];
         }
     }
     __syncthreads();
     // per token, the rows of the tiles that kept it, in ascending tile order
-    for (int32_t j = warp; j < kBlockTok; j += kThreads / 32) {
+    for (int32_t j = warp; j < kRunTok; j += kRunThreads / 32) {
         int32_t len = 0;
         for (int32_t t0 = 0; t0 < nt; t0 += 32) {
             const int32_t t = t0 + lane;
-            const int32_t sl = t < nt ? sm.slot[t][j] : -1;
+            const int32_t sl = t < nt ? s_slot[t * (kRunTok + 1) + j] : -1;
             const uint32_t m = __ballot_sync(0xffffffffu, sl >= 0 && sl < ncap);
             if ((m >> lane) & 1u)
-                sm.row[j][len + __popc(m & ((1u << lane) - 1u))] = ((uint32_t)t * g.B + b) * (uint32_t)ncap + sl;
+                s_row[j * nt + len + __popc(m & ((1u << lane) - 1u))] = ((uint32_t)t * g.B + b) * (uint32_t)ncap + sl;
             len += __popc(m);
         }
-        if (lane == 0) sm.len[j] = len;
+        if (lane == 0) s_len[j] = k0 + j < N ? len : -1;
     }
     __syncthreads();
-    const int32_t groups = kThreads / lpt, grp = threadIdx.x / lpt, gl = threadIdx.x - grp * lpt;
-    // light tokens: a group of lpt lanes per token, rows summed one by one in list order
-    for (int32_t j = grp; j < kBlockTok && k0 + j < N; j += groups) {
-        const int32_t len = sm.len[j];
-        if (len > kLightRows) continue;
-        const int64_t tok = (int64_t)b * N + k0 + j;
-        for (int32_t cv = gl; cv < CV; cv += lpt) {
-            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            for (int32_t i0 = 0; i0 < len; i0 += kListRows) cond_rows<BF16>(sm, Ycond, CV, cv, j, i0, len, acc);
-            __stcs(out + tok * CV + cv, len > 0 ? acc_div<BF16>(acc, (float)len) : make_uint4(0u, 0u, 0u, 0u));
+    // runs: a token has max(1, ceil(len / kRunRows)) of them (a token no tile kept has one
+    // empty run, which writes its zeros); numbered token after token
+    if (warp == 0) {
+        const int32_t len = lane < kRunTok ? s_len[lane] : -1;
+        const int32_t nr = len < 0 ? 0 : max(1, (len + kRunRows - 1) / kRunRows);
+        int32_t sc = nr;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, sc, o);
+            if (lane >= o) sc += y;
         }
+        if (lane < kRunTok) s_run0[lane] = sc - nr;
+        if (lane == 31) s_run0[kRunTok] = sc;
     }
-    // heavy tokens: the whole block; group q sums run q of kListRows consecutive rows,
-    // group 0 adds the runs' sums in order
-    for (int32_t j = 0; j < kBlockTok && k0 + j < N; ++j) {
-        const int32_t len = sm.len[j];                // block-uniform
-        if (len <= kLightRows) continue;
-        const int64_t tok = (int64_t)b * N + k0 + j;
-        for (int32_t cv0 = 0; cv0 < CV; cv0 += lpt) {
-            const int32_t cv = cv0 + gl;
-            const bool act = cv < CV;
-            float tot[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            for (int32_t r0 = 0; r0 < len; r0 += groups * kListRows) {
+    __syncthreads();
+    for (int32_t j = warp; j < kRunTok; j += kRunThreads / 32) {
+        const int32_t r0 = s_run0[j], nr = s_run0[j + 1] - r0;
+        for (int32_t r = lane; r < nr; r += 32) s_tab[r0 + r] = (uint16_t)((j << 8) | r);
+    }
+    __syncthreads();
+    // chunks of P runs: group q of lpt lanes sums runs c0 + q, c0 + q + G, ... one after
+    // another, with no barrier between them.  A token with one run is written by its group;
+    // the run sums of a token with more are kept in shared memory, and after the chunk one
+    // group per such token adds them in order to the carry of the chunks before.
+    const int32_t U = s_run0[kRunTok];
+    const int32_t G = kRunThreads / lpt, grp = threadIdx.x / lpt, gl = threadIdx.x - grp * lpt;
+    const int32_t P = kPartFloats / (8 * lpt);
+    for (int32_t cv0 = 0; cv0 < CV; cv0 += lpt) {
+        const int32_t cv = cv0 + gl;
+        const bool act = cv < CV;
+        for (int32_t c0 = 0, ci = 0; c0 < U; c0 += P, ++ci) {
+            const int32_t c1 = min(U, c0 + P);
+            for (int32_t u = c0 + grp; u < c1; u += G) {
+                const uint32_t e = s_tab[u];
+                const int32_t j = (int32_t)(e >> 8), len = s_len[j];
                 float part[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                if (act) cond_rows<BF16>(sm, Ycond, CV, cv, j, r0 + grp * kListRows, len, part);
+                if (act) run_rows<BF16>(s_row + j * nt, Ycond, CV, cv, (int32_t)(e & 255u) * kRunRows, len, part);
+                if (s_run0[j + 1] - s_run0[j] == 1) {
+                    if (act)
+                        __stcs(out + ((int64_t)b * N + k0 + j) * CV + cv,
+                               len > 0 ? acc_div<BF16>(part, (float)len) : make_uint4(0u, 0u, 0u, 0u));
+                } else {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) sm.part[e][threadIdx.x] = part[e];
-                __syncthreads();
-                if (grp == 0 && act) {
-                    for (int32_t q = 0; q < groups && r0 + q * kListRows < len; ++q) {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) tot[e] += sm.part[e][q * lpt + gl];
-                    }
+                    for (int x = 0; x < 8; ++x) s_part[(x * P + (u - c0)) * lpt + gl] = part[x];
                 }
-                __syncthreads();
             }
-            if (grp == 0 && act) __stcs(out + tok * CV + cv, acc_div<BF16>(tot, (float)len));
+            __syncthreads();
+            const int32_t ja = (int32_t)(s_tab[c0] >> 8), jb = (int32_t)(s_tab[c1 - 1] >> 8);
+            for (int32_t j = ja + grp; j <= jb; j += G) {
+                const int32_t rs = s_run0[j], re = s_run0[j + 1];
+                if (re - rs <= 1) continue;
+                float acc[8];
+                const float *cin = s_carry + ((ci + 1) & 1) * 256;
+#pragma unroll
+                for (int x = 0; x < 8; ++x) acc[x] = rs < c0 ? cin[x * 32 + gl] : 0.f;
+                const int32_t qe = min(re, c1);
+                for (int32_t q = max(rs, c0); q < qe; ++q) {
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) acc[x] += s_part[(x * P + (q - c0)) * lpt + gl];
+                }
+                if (re <= c1) {
+                    if (act) __stcs(out + ((int64_t)b * N + k0 + j) * CV + cv, acc_div<BF16>(acc, (float)s_len[j]));
+                } else {
+                    float *cout = s_carry + (ci & 1) * 256;
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) cout[x * 32 + gl] = acc[x];
+                }
+            }
+            __syncthreads();
         }
     }
 }
@@ -281,15 +356,16 @@ extern "C" tdp_status tdp_cond_blend(tdp_plan_t plan, int32_t N, int32_t ncap, c
     uint4 *o = reinterpret_cast<uint4 *>(out);
     cudaError_t err;
     if (g.nt <= kStageTiles && (uint64_t)g.nt * (uint64_t)g.B * (uint64_t)ncap <= 0xffffffffull) {
-        const int64_t blocks = (int64_t)g.B * ((N + kBlockTok - 1) / kBlockTok);
+        const int64_t blocks = (int64_t)g.B * ((N + kRunTok - 1) / kRunTok);
         if (blocks > 0x7fffffffLL) return tdp_fail(TDP_ERR_TOO_LARGE, "cond blend grid too large");
         int32_t lpt = 1;                                      // lanes per token: CV rounded up to 2^k, <= 32
         while (lpt < CV && lpt < 32) lpt *= 2;
+        const size_t smem = run_layout(g.nt).bytes;
         err = g.dtype == TDP_BF16
-                  ? tdp_launch(true, tdp_cond_blend_staged_kernel<1>, (unsigned)blocks, kThreads, s, g, N, ncap, CV,
-                               lpt, y, slot, o)
-                  : tdp_launch(true, tdp_cond_blend_staged_kernel<0>, (unsigned)blocks, kThreads, s, g, N, ncap, CV,
-                               lpt, y, slot, o);
+                  ? tdp_launch_smem(true, tdp_cond_blend_runs_kernel<1>, (unsigned)blocks, kRunThreads, smem, s, g, N,
+                                    ncap, CV, lpt, y, slot, o)
+                  : tdp_launch_smem(true, tdp_cond_blend_runs_kernel<0>, (unsigned)blocks, kRunThreads, smem, s, g, N,
+                                    ncap, CV, lpt, y, slot, o);
     } else {
         const int64_t warps = (int64_t)g.B * N;              // one warp per conditioning token
         const int64_t blocks = (warps + kThreads / 32 - 1) / (kThreads / 32);

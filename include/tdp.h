@@ -230,8 +230,8 @@ tdp_status tdp_split_filter(tdp_plan_t plan, const void *X, const int32_t *P, co
  *
  * out[b,k,:] = (1/n) * sum over the tiles t that kept token k of
  * Ycond[t,b,slot[t,b,k],:], n = number of those tiles; fp32 accumulation in
- * ascending t (for n > 16: sums of runs of 8 consecutive kept tiles, added in
- * order), one division per element by n, stored in the plan's dtype.  A token
+ * ascending t, in runs of 8 consecutive kept tiles whose sums are added in
+ * order, one division per element by n, stored in the plan's dtype.  A token
  * that no tile kept gets 0.
  *
  *   N      conditioning tokens per batch item (>= 0).
