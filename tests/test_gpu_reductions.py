@@ -113,3 +113,20 @@ def test_cond_blend_tile_count_edges(tdp, nw):
     wl = wk.by_name("tiny").replace(F=2, H=48, W=52, C=8, dtype="bf16", num_tiles=(1, 16, nw),
                                     overlap=(0, 1, 1), n_cond=200)
     _cond_case(tdp, wl)
+
+
+def test_cond_blend_runs_across_chunks(tdp):
+    """256 tiles and 1 KB rows (bf16 C=512: 64 vectors, two passes of 32 lanes): a token
+    kept by every tile has 32 runs of 8 rows, more than one chunk of run sums holds, so
+    its sum is carried from chunk to chunk; half the tokens have negative time."""
+    wl = wk.by_name("tiny").replace(F=2, H=48, W=52, C=512, dtype="bf16", num_tiles=(1, 16, 16),
+                                    overlap=(0, 1, 1), n_cond=120, neg_frac=0.5)
+    out, _, _ = _cond_case(tdp, wl)
+    assert int(out["kcount"].max()) == 256
+
+
+def test_cond_blend_odd_vector_count(tdp):
+    """bf16 C=136: 17 channel vectors, so 15 of a token's 32 lanes have no vector."""
+    wl = wk.by_name("tiny").replace(F=4, H=24, W=40, C=136, dtype="bf16", num_tiles=(2, 4, 8),
+                                    overlap=(1, 2, 2), n_cond=400)
+    _cond_case(tdp, wl)
