@@ -109,7 +109,7 @@ def test_cond_blend_wide_channels(tdp):
 
 @pytest.mark.parametrize("nw", [16, 17])
 def test_cond_blend_tile_count_edges(tdp, nw):
-    """256 tiles (the largest count the staged kernel takes) and 272 (the warp-per-token kernel)."""
+    """256 tiles (the largest count the run kernel takes) and 272 (the warp-per-token kernel)."""
     wl = wk.by_name("tiny").replace(F=2, H=48, W=52, C=8, dtype="bf16", num_tiles=(1, 16, nw),
                                     overlap=(0, 1, 1), n_cond=200)
     _cond_case(tdp, wl)
