@@ -96,6 +96,9 @@ def test_plan_matches_oracle_sweep(tdp):
     (dict(W=200, num_tiles=(1, 1, 65), overlap=(0, 0, 0)), 5),
     (dict(B=-1), 1),
     (dict(F=0), 1),
+    (dict(F=(1 << 25) + 1, num_tiles=(1, 1, 1), overlap=(0, 0, 0)), 5),       # a dimension past 2^25
+    (dict(B=1 << 16, F=256, H=256, num_tiles=(1, 1, 1), overlap=(0, 0, 0)), 5),   # B*F*H rows past 2^31
+    (dict(B=1 << 13, F=64, H=64, W=64, num_tiles=(64, 64, 64), overlap=(0, 0, 0)), 5),  # nt*B*3 past 2^31
 ])
 def test_plan_rejects_invalid(tdp, kw, status):
     base = dict(B=1, F=3, H=8, W=12, C=16, dtype="f32", num_tiles=(1, 2, 2), overlap=(0, 2, 2))
