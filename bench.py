@@ -48,7 +48,8 @@ LAUNCHES_PER_STEP = {
     "fused": 4,       # bounds init, bounds, split + filter, blend
     "separate": 6,    # bounds init, bounds, split, keep, compact, blend
 }
-PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "dram_traffic_large.txt")
+# ncu DRAM-traffic summaries, one per workload: profiles/dram_traffic_<workload>.txt
+PROFILE_DIR = os.path.join(ROOT, "profiles")
 INSTRUMENT_EVERY = 10        # steps between those timed call by call
 
 
@@ -206,12 +207,13 @@ CALL_KERNELS = {
 }
 
 
-def profiled_traffic(call):
-    """DRAM bytes (read + write) of one `call`, summed over its kernels, from the committed
-    ncu summary; None when a kernel's sources changed since the capture (or none was taken)."""
+def profiled_traffic(call, workload=WORKLOAD):
+    """DRAM bytes (read + write) of one `call` on `workload`, summed over its kernels, from
+    the committed ncu summary of that workload; None when none was taken for it, or when a
+    kernel's sources changed since the capture."""
     rows = {}
     try:
-        with open(PROFILE_TRAFFIC) as fh:
+        with open(os.path.join(PROFILE_DIR, f"dram_traffic_{workload}.txt")) as fh:
             for line in fh:
                 parts = line.split()
                 if parts and not line.startswith("#"):
@@ -555,7 +557,7 @@ def run_ours(args, rank, world, local_rank):
             "tdp_split_filter (tdp_bounds_init_kernel + tdp_bounds_kernel + tdp_split_filter_kernel)",
             "kernels": CALL_KERNELS[call], "achieved": kern[dom]["GB/s"], "peak": peak,
             "peak_kind": f"{peak_kind} copy bandwidth", "unit": "GB/s", "frac": kern[dom]["GB/s"] / peak,
-            "traffic": profiled_traffic(call), "algorithmic_bytes_per_launch": kern[dom]["algorithmic_bytes"],
+            "traffic": profiled_traffic(call, wl.name), "algorithmic_bytes_per_launch": kern[dom]["algorithmic_bytes"],
             "frac_of_nominal_8tbs": kern[dom]["GB/s"] / NOMINAL_HBM_GBS}
     value = world * ab["step"] / (ms * 1e-3) / 1e9
     line = {

@@ -64,7 +64,7 @@ def test_traffic_file_parser(tmp_path, monkeypatch):
         f"{k} {h} {100 + i} {10 + i} 5 0" for i, (k, h) in enumerate(sorted(rows.items()))) + "\n"
     f = tmp_path / "dram_traffic_large.txt"
     f.write_text(text)
-    monkeypatch.setattr(bench, "PROFILE_TRAFFIC", str(f))
+    monkeypatch.setattr(bench, "PROFILE_DIR", str(tmp_path))
     order = sorted(rows)
     expect = {k: 100 + i + 10 + i for i, k in enumerate(order)}
     assert bench.profiled_traffic("tdp_blend") == expect["tdp_blend_kernel"]
@@ -75,15 +75,26 @@ def test_traffic_file_parser(tmp_path, monkeypatch):
     assert bench.profiled_traffic("tdp_blend") is None
     f.write_text("# nothing captured\n")
     assert bench.profiled_traffic("tdp_split_filter") is None
+    # another workload has no capture of its own: no figure, not the large workload's
+    f.write_text(text)
+    assert bench.profiled_traffic("tdp_blend", "large") == expect["tdp_blend_kernel"]
+    assert bench.profiled_traffic("tdp_blend", "temporal") is None
 
 
-def test_committed_traffic_file_parses():
-    """Every line of the committed file has a kernel the bench knows and integer fields."""
-    lines = [ln.split() for ln in open(bench.PROFILE_TRAFFIC) if ln.strip() and not ln.startswith("#")]
-    assert lines
-    for parts in lines:
-        assert parts[0] in bench.KERNEL_SOURCES and len(parts[1]) == 16
-        assert all(np.int64(int(x)) >= 0 for x in parts[2:6])
+def test_committed_traffic_files_parse():
+    """Every committed traffic file is named for a workload, and every line of it has a kernel
+    the bench knows and integer fields."""
+    import glob
+    names = {w.name for w in bench.wk.WORKLOADS}
+    files = glob.glob(os.path.join(bench.PROFILE_DIR, "dram_traffic_*.txt"))
+    assert files
+    for path in files:
+        assert os.path.basename(path)[len("dram_traffic_"):-len(".txt")] in names
+        lines = [ln.split() for ln in open(path) if ln.strip() and not ln.startswith("#")]
+        assert lines
+        for parts in lines:
+            assert parts[0] in bench.KERNEL_SOURCES and len(parts[1]) == 16
+            assert all(np.int64(int(x)) >= 0 for x in parts[2:6])
 
 
 def test_reference_arm_under_torchrun_prints_one_line():
