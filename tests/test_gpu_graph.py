@@ -1,4 +1,5 @@
-"""One TDP step (bounds, split, filter, blend; as separate calls or with tdp_split_filter) captured in a CUDA graph and replayed gives
+"""One TDP step (bounds, split, filter, blend; as separate calls or with tdp_split_filter;
+then the conditioning blend and the tile mean) captured in a CUDA graph and replayed gives
 the same bytes as the same calls launched directly: the library allocates nothing and
 never synchronises, so its calls can sit inside a captured per-step graph."""
 import numpy as np
@@ -23,15 +24,21 @@ def test_graph_replay_matches_direct_launches(fused):
     N = K.shape[2]
     Xd, Pd, Kd = to_dev(X), to_dev(P), to_dev(K)
     Yout = torch.randn((plan.total_tile_tokens, wl.C), device="cuda").to(torch.bfloat16)
+    ncap = N                                   # rows reserved per tile: every kept token fits
+    Ycond = torch.randn((plan.n_tiles, wl.B, ncap, wl.C), device="cuda").to(torch.bfloat16)
+    La = 1000 * wl.C
+    A = torch.randn((plan.n_tiles, wl.B, La), device="cuda").to(torch.bfloat16)
 
     def buffers():
         Y, Q, mn, mx = tdp.alloc_split_outputs(plan, "cuda")
         f = tdp.alloc_filter_outputs(plan, N, "cuda", slot=True)
         Z = torch.empty_like(Xd)
-        return [Y, Q, mn, mx, *f, Z]
+        Oc = torch.empty((wl.B, N, wl.C), dtype=torch.bfloat16, device="cuda")
+        Om = torch.empty((wl.B, La), dtype=torch.bfloat16, device="cuda")
+        return [Y, Q, mn, mx, *f, Z, Oc, Om]
 
     def step(b, s):
-        Y, Q, mn, mx, keep, idx, count, kcount, Kout, slot, Z = b
+        Y, Q, mn, mx, keep, idx, count, kcount, Kout, slot, Z, Oc, Om = b
         if fused:
             tdp.tdp_split_filter(plan, Xd, Pd, Kd, N, 1, Y, Q, mn, mx, keep, idx, count, kcount, Kout, slot,
                                  stream=s)
@@ -40,6 +47,8 @@ def test_graph_replay_matches_direct_launches(fused):
             tdp.tdp_split(plan, Xd, Pd, mn, 1, Y, Q, stream=s)
             tdp.tdp_norm_filter(plan, Kd, N, mn, mx, 1, keep, idx, count, kcount, Kout, slot, stream=s)
         tdp.tdp_blend(plan, Yout, Z, stream=s)
+        tdp.tdp_cond_blend(plan, N, ncap, Ycond, slot, Oc, stream=s)
+        tdp.tdp_tile_mean(plan, La, A, Om, stream=s)
 
     s = torch.cuda.Stream()
     direct, graphed = buffers(), buffers()
@@ -58,7 +67,7 @@ def test_graph_replay_matches_direct_launches(fused):
     for _ in range(2):
         g.replay()
     torch.cuda.synchronize()
-    names = ["Y", "Q", "mn", "mx", "keep", "idx", "count", "kcount", "Kout", "slot", "Z"]
+    names = ["Y", "Q", "mn", "mx", "keep", "idx", "count", "kcount", "Kout", "slot", "Z", "cond", "mean"]
     for name, a, b in zip(names, direct, graphed):
         if name == "Kout":   # entries past count are unspecified: compare the kept ones
             c = direct[6].cpu().numpy()
