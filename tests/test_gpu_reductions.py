@@ -96,8 +96,9 @@ def test_cond_blend_many_tiles(tdp):
 
 
 def test_cond_blend_ragged_tokens(tdp):
-    """Token counts that leave the last block of 32 tokens part-filled, two batch items."""
-    _cond_case(tdp, wk.by_name("small").replace(B=2, n_cond=1000))
+    """A token count that is not a multiple of 8, 16 or 32 (the last block of tokens of each
+    batch item is part-filled), two batch items."""
+    _cond_case(tdp, wk.by_name("small").replace(B=2, n_cond=1003))
 
 
 def test_cond_blend_wide_channels(tdp):
