@@ -123,3 +123,53 @@ print("ok")
     root = __import__("os").path.dirname(__import__("os").path.dirname(__import__("os").path.abspath(__file__)))
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=600, cwd=root)
     assert r.returncode == 0 and r.stdout.strip().endswith("ok"), (r.stdout[-2000:], r.stderr[-3000:])
+
+
+def test_graph_split_model_blend():
+    """A denoising step as a captured graph: tdp_split_filter, a stand-in per-tile model (a
+    torch elementwise update of the tiles, as the transformer would run between the two
+    calls), then tdp_blend; the replay matches the same work launched directly."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import blend_tdp_tile_gb300 as tdp
+    wl = wk.by_name("medium")
+    X, P, K = wk.make_inputs(wl)
+    plan = tdp.tdp_plan_create(wl.B, wl.F, wl.H, wl.W, wl.C, wl.dtype, wl.num_tiles, wl.overlap)
+    N = K.shape[2]
+    Xd, Pd, Kd = to_dev(X), to_dev(P), to_dev(K)
+    noise = (0.05 * torch.randn((plan.total_tile_tokens, wl.C), device="cuda")).to(torch.bfloat16)
+
+    def buffers():
+        Y, Q, mn, mx = tdp.alloc_split_outputs(plan, "cuda")
+        return [Y, Q, mn, mx, *tdp.alloc_filter_outputs(plan, N, "cuda", slot=True), torch.empty_like(Xd)]
+
+    def step(b, s):
+        Y, Q, mn, mx, keep, idx, count, kcount, Kout, slot, Z = b
+        tdp.tdp_split_filter(plan, Xd, Pd, Kd, N, 1, Y, Q, mn, mx, keep, idx, count, kcount, Kout, slot,
+                             stream=s)
+        with torch.cuda.stream(s):
+            Y.mul_(0.5).add_(noise)            # the per-tile model's stand-in, on the same stream
+        tdp.tdp_blend(plan, Y, Z, stream=s)
+
+    s = torch.cuda.Stream()
+    direct, graphed = buffers(), buffers()
+    step(direct, s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step(graphed, s)
+    for t in graphed:
+        t.zero_()
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    Zd, Zg = direct[-1], graphed[-1]
+    assert torch.equal(Zd.view(torch.int16), Zg.view(torch.int16))
+    # and the blend of the halved tiles plus noise is half the latent plus the blended noise
+    Zn = torch.empty_like(Xd)
+    tdp.tdp_blend(plan, noise, Zn)
+    torch.cuda.synchronize()
+    ref = 0.5 * Xd.float() + Zn.float()
+    assert ((Zd.float() - ref).abs() <= 2e-2 + 1e-2 * ref.abs()).all()   # bf16 roundings of the update and of Z
