@@ -190,3 +190,35 @@ def test_zero_batch_is_a_no_op(tdp):
     vp = ctypes.c_void_p
     lib.tdp_blend.argtypes = [vp, vp, vp, vp]
     assert lib.tdp_blend(plan.handle, None, None, None) == 0
+
+
+def test_threads_share_a_plan_and_keep_their_own_error_detail(tdp):
+    """A plan is immutable and usable from any host thread; the error detail is per thread."""
+    import threading
+    plan = tdp.tdp_plan_create(1, 16, 32, 48, 128, "bf16", (1, 2, 2), (0, 8, 8))
+    ref = tdp.tdp_plan_info(plan)
+    errors = []
+
+    def worker(i):
+        try:
+            for _ in range(200):
+                n, tot, boxes, offs = tdp.tdp_plan_info(plan)
+                assert n == ref[0] and tot == ref[1]
+                assert np.array_equal(boxes, ref[2]) and np.array_equal(offs, ref[3])
+                assert list(tdp.tdp_rank_tiles(plan, i % 4, 4)) == list(range(i % 4, n, 4))
+                bad = dict(C=6) if i % 2 else dict(num_tiles=(1, 99, 1))
+                with pytest.raises(tdp.TdpError) as ei:
+                    tdp.tdp_plan_create(1, 3, 8, 12, bad.get("C", 16), "bf16", bad.get("num_tiles", (1, 2, 2)),
+                                        (0, 2, 2))
+                detail = tdp.tdp_last_error_detail()
+                assert ("multiple of 16" in detail) if i % 2 else ("multiple of 16" not in detail and detail)
+                assert ei.value.status == (4 if i % 2 else 2)
+        except Exception as e:        # reported by the main thread
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(8)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors[:3]

@@ -173,3 +173,47 @@ def test_graph_split_model_blend():
     torch.cuda.synchronize()
     ref = 0.5 * Xd.float() + Zn.float()
     assert ((Zd.float() - ref).abs() <= 2e-2 + 1e-2 * ref.abs()).all()   # bf16 roundings of the update and of Z
+
+
+def test_one_plan_two_streams_two_threads():
+    """One plan used at once from two host threads, each with its own stream and buffers:
+    every result equals the same work launched alone."""
+    import threading
+
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import blend_tdp_tile_gb300 as tdp
+    wl = wk.by_name("medium")
+    X, P, K = wk.make_inputs(wl)
+    plan = tdp.tdp_plan_create(wl.B, wl.F, wl.H, wl.W, wl.C, wl.dtype, wl.num_tiles, wl.overlap)
+    N = K.shape[2]
+    Pd, Kd = to_dev(P), to_dev(K)
+    lat = [to_dev(X), -to_dev(X)]                       # two different latents
+
+    def run(i, s, out, reps):
+        Y, Q, mn, mx = tdp.alloc_split_outputs(plan, "cuda")
+        f = tdp.alloc_filter_outputs(plan, N, "cuda", slot=True)
+        Z = torch.empty_like(lat[i])
+        with torch.cuda.stream(s):
+            for _ in range(reps):
+                tdp.tdp_split_filter(plan, lat[i], Pd, Kd, N, 1, Y, Q, mn, mx, *f, stream=s)
+                tdp.tdp_blend(plan, Y, Z, stream=s)
+        s.synchronize()
+        out[i] = (Y.view(torch.int16).clone(), Q.clone(), Z.view(torch.int16).clone(), f[1].clone())
+
+    alone = [None, None]
+    for i in range(2):
+        run(i, torch.cuda.Stream(), alone, 1)
+    together = [None, None]
+    threads = [threading.Thread(target=run, args=(i, torch.cuda.Stream(), together, 20)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    for i in range(2):
+        assert together[i] is not None
+        for a, b in zip(alone[i], together[i]):
+            assert torch.equal(a, b)
+    assert torch.equal(alone[0][2], lat[0].view(torch.int16))   # blend(split(X)) == X
