@@ -222,17 +222,61 @@ def _ptr(t, name, numel, dtypes, align):
     return p
 
 
+def _common_device(where, named):
+    """The one device every given buffer lives on (None if no buffer is given).
+
+    The library launches on the current CUDA device, so buffers of one call must share a
+    device: a pointer of another device would reach the kernel as a foreign address.
+    `named` holds (name, tensor-or-None) pairs; only `.device` of each is read."""
+    dev, first = None, None
+    for name, t in named:
+        if t is None:
+            continue
+        if dev is None:
+            dev, first = t.device, name
+        elif t.device != dev:
+            raise ValueError(f"{where}: {name} is on {t.device} but {first} is on {dev}")
+    return dev
+
+
+def _stream_handle(where, stream, dev):
+    """Raw cudaStream_t for `stream` on device `dev`: None -> that device's current torch
+    stream; a torch stream must belong to `dev`; an int is taken as a raw handle."""
+    if stream is None:
+        return _torch().cuda.current_stream(dev).cuda_stream
+    if isinstance(stream, int):
+        return stream
+    sdev = getattr(stream, "device", None)
+    if dev is not None and sdev is not None and sdev != dev:
+        raise ValueError(f"{where}: stream is on {sdev} but the buffers are on {dev}")
+    return stream.cuda_stream
+
+
+class _Call:
+    """Marshals one entry-point call: checks each buffer (size, dtype, contiguity,
+    alignment, one common device), then calls the library with that device current."""
+
+    def __init__(self, where):
+        self.where = where
+        self.named = []
+
+    def ptr(self, t, name, numel, dtypes, align):
+        p = _ptr(t, name, numel, dtypes, align)
+        self.named.append((name, t))
+        return p
+
+    def run(self, fn, *args, stream=None):
+        torch = _torch()
+        dev = _common_device(self.where, self.named)
+        if dev is None:
+            dev = torch.device("cuda", torch.cuda.current_device())
+        with torch.cuda.device(dev):
+            _check(fn(*args, _stream_handle(self.where, stream, dev)), self.where)
+
+
 def _latent_dtypes(plan):
     torch = _torch()
     return (torch.float32,) if plan.dtype == TDP_F32 else (torch.bfloat16,)
-
-
-def _stream(stream):
-    if stream is None:
-        return _torch().cuda.current_stream().cuda_stream
-    if isinstance(stream, int):
-        return stream
-    return stream.cuda_stream
 
 
 def tdp_pos_bounds(plan: Plan, P, mn, mx, stream=None):
@@ -240,9 +284,9 @@ def tdp_pos_bounds(plan: Plan, P, mn, mx, stream=None):
     torch = _torch()
     B, T, nt = plan.B, plan.F * plan.H * plan.W, plan.n_tiles
     i32 = (torch.int32,)
-    _check(_lib.tdp_pos_bounds(plan.handle, _ptr(P, "P", B * 3 * T * 2, i32, 8),
-                               _ptr(mn, "mn", nt * B * 3, i32, 4), _ptr(mx, "mx", nt * B * 3, i32, 4),
-                               _stream(stream)), "tdp_pos_bounds")
+    c = _Call("tdp_pos_bounds")
+    c.run(_lib.tdp_pos_bounds, plan.handle, c.ptr(P, "P", B * 3 * T * 2, i32, 8),
+          c.ptr(mn, "mn", nt * B * 3, i32, 4), c.ptr(mx, "mx", nt * B * 3, i32, 4), stream=stream)
 
 
 def tdp_split(plan: Plan, X, P, mn, normalize, Y, Q, stream=None):
@@ -251,16 +295,14 @@ def tdp_split(plan: Plan, X, P, mn, normalize, Y, Q, stream=None):
     torch = _torch()
     B, T, C, nt, tot = plan.B, plan.F * plan.H * plan.W, plan.C, plan.n_tiles, plan.total_tile_tokens
     lat = _latent_dtypes(plan)
-    args = (
-        _ptr(X, "X", B * T * C, lat, 16),
-        _ptr(P, "P", B * 3 * T * 2, (torch.int32,), 8),
-        _ptr(mn, "mn", nt * B * 3, (torch.int32,), 4),
-        int(bool(normalize)),
-        _ptr(Y, "Y", B * tot * C, lat, 16),
-        _ptr(Q, "Q", B * tot * 6, (torch.int32,), 8),
-        _stream(stream),
-    )
-    _check(_lib.tdp_split(plan.handle, *args), "tdp_split")
+    c = _Call("tdp_split")
+    c.run(_lib.tdp_split, plan.handle,
+          c.ptr(X, "X", B * T * C, lat, 16),
+          c.ptr(P, "P", B * 3 * T * 2, (torch.int32,), 8),
+          c.ptr(mn, "mn", nt * B * 3, (torch.int32,), 4),
+          int(bool(normalize)),
+          c.ptr(Y, "Y", B * tot * C, lat, 16),
+          c.ptr(Q, "Q", B * tot * 6, (torch.int32,), 8), stream=stream)
 
 
 def tdp_norm_filter(plan: Plan, K, N, mn, mx, normalize, keep, idx, count, kcount, Kout, slot=None,
@@ -271,20 +313,18 @@ def tdp_norm_filter(plan: Plan, K, N, mn, mx, normalize, keep, idx, count, kcoun
     B, nt = plan.B, plan.n_tiles
     N = int(N)
     i32 = (torch.int32,)
-    args = (
-        _ptr(K, "K", B * 3 * N * 2, i32, 8), N,
-        _ptr(mn, "mn", nt * B * 3, i32, 4),
-        _ptr(mx, "mx", nt * B * 3, i32, 4),
-        int(bool(normalize)),
-        _ptr(keep, "keep", nt * B * N, (torch.uint8,), 1),
-        _ptr(idx, "idx", nt * B * N, i32, 4),
-        _ptr(count, "count", nt * B, i32, 4),
-        _ptr(kcount, "kcount", B * N, i32, 4),
-        _ptr(Kout, "Kout", nt * B * 3 * N * 2, i32, 8),
-        _ptr(slot, "slot", nt * B * N, i32, 4),
-        _stream(stream),
-    )
-    _check(_lib.tdp_norm_filter(plan.handle, *args), "tdp_norm_filter")
+    c = _Call("tdp_norm_filter")
+    c.run(_lib.tdp_norm_filter, plan.handle,
+          c.ptr(K, "K", B * 3 * N * 2, i32, 8), N,
+          c.ptr(mn, "mn", nt * B * 3, i32, 4),
+          c.ptr(mx, "mx", nt * B * 3, i32, 4),
+          int(bool(normalize)),
+          c.ptr(keep, "keep", nt * B * N, (torch.uint8,), 1),
+          c.ptr(idx, "idx", nt * B * N, i32, 4),
+          c.ptr(count, "count", nt * B, i32, 4),
+          c.ptr(kcount, "kcount", B * N, i32, 4),
+          c.ptr(Kout, "Kout", nt * B * 3 * N * 2, i32, 8),
+          c.ptr(slot, "slot", nt * B * N, i32, 4), stream=stream)
 
 
 def tdp_split_filter(plan: Plan, X, P, K, N, normalize, Y, Q, mn, mx, keep, idx, count, kcount, Kout,
@@ -296,24 +336,22 @@ def tdp_split_filter(plan: Plan, X, P, K, N, normalize, Y, Q, mn, mx, keep, idx,
     N = int(N)
     lat = _latent_dtypes(plan)
     i32 = (torch.int32,)
-    args = (
-        _ptr(X, "X", B * T * C, lat, 16),
-        _ptr(P, "P", B * 3 * T * 2, i32, 8),
-        _ptr(K, "K", B * 3 * N * 2, i32, 8), N,
-        int(bool(normalize)),
-        _ptr(Y, "Y", B * tot * C, lat, 16),
-        _ptr(Q, "Q", B * tot * 6, i32, 8),
-        _ptr(mn, "mn", nt * B * 3, i32, 4),
-        _ptr(mx, "mx", nt * B * 3, i32, 4),
-        _ptr(keep, "keep", nt * B * N, (torch.uint8,), 1),
-        _ptr(idx, "idx", nt * B * N, i32, 4),
-        _ptr(count, "count", nt * B, i32, 4),
-        _ptr(kcount, "kcount", B * N, i32, 4),
-        _ptr(Kout, "Kout", nt * B * 3 * N * 2, i32, 8),
-        _ptr(slot, "slot", nt * B * N, i32, 4),
-        _stream(stream),
-    )
-    _check(_lib.tdp_split_filter(plan.handle, *args), "tdp_split_filter")
+    c = _Call("tdp_split_filter")
+    c.run(_lib.tdp_split_filter, plan.handle,
+          c.ptr(X, "X", B * T * C, lat, 16),
+          c.ptr(P, "P", B * 3 * T * 2, i32, 8),
+          c.ptr(K, "K", B * 3 * N * 2, i32, 8), N,
+          int(bool(normalize)),
+          c.ptr(Y, "Y", B * tot * C, lat, 16),
+          c.ptr(Q, "Q", B * tot * 6, i32, 8),
+          c.ptr(mn, "mn", nt * B * 3, i32, 4),
+          c.ptr(mx, "mx", nt * B * 3, i32, 4),
+          c.ptr(keep, "keep", nt * B * N, (torch.uint8,), 1),
+          c.ptr(idx, "idx", nt * B * N, i32, 4),
+          c.ptr(count, "count", nt * B, i32, 4),
+          c.ptr(kcount, "kcount", B * N, i32, 4),
+          c.ptr(Kout, "Kout", nt * B * 3 * N * 2, i32, 8),
+          c.ptr(slot, "slot", nt * B * N, i32, 4), stream=stream)
 
 
 def tdp_cond_blend(plan: Plan, N, ncap, Ycond, slot, out, stream=None):
@@ -323,25 +361,28 @@ def tdp_cond_blend(plan: Plan, N, ncap, Ycond, slot, out, stream=None):
     B, nt, C = plan.B, plan.n_tiles, plan.C
     N, ncap = int(N), int(ncap)
     lat = _latent_dtypes(plan)
-    _check(_lib.tdp_cond_blend(plan.handle, N, ncap, _ptr(Ycond, "Ycond", nt * B * ncap * C, lat, 16),
-                               _ptr(slot, "slot", nt * B * N, (torch.int32,), 4),
-                               _ptr(out, "out", B * N * C, lat, 16), _stream(stream)), "tdp_cond_blend")
+    c = _Call("tdp_cond_blend")
+    c.run(_lib.tdp_cond_blend, plan.handle, N, ncap, c.ptr(Ycond, "Ycond", nt * B * ncap * C, lat, 16),
+          c.ptr(slot, "slot", nt * B * N, (torch.int32,), 4),
+          c.ptr(out, "out", B * N * C, lat, 16), stream=stream)
 
 
 def tdp_tile_mean(plan: Plan, L, A, out, stream=None):
     """Mean over tiles of A [nt,B,L] into out [B,L] (the audio path)."""
     B, nt, L = plan.B, plan.n_tiles, int(L)
     lat = _latent_dtypes(plan)
-    _check(_lib.tdp_tile_mean(plan.handle, L, _ptr(A, "A", nt * B * L, lat, 16),
-                              _ptr(out, "out", B * L, lat, 16), _stream(stream)), "tdp_tile_mean")
+    c = _Call("tdp_tile_mean")
+    c.run(_lib.tdp_tile_mean, plan.handle, L, c.ptr(A, "A", nt * B * L, lat, 16),
+          c.ptr(out, "out", B * L, lat, 16), stream=stream)
 
 
 def tdp_blend(plan: Plan, Yout, Z, stream=None):
     """Blend tile-major tile outputs Yout into Z [B,F,H,W,C] with the trapezoidal masks."""
     B, T, C, tot = plan.B, plan.F * plan.H * plan.W, plan.C, plan.total_tile_tokens
     lat = _latent_dtypes(plan)
-    _check(_lib.tdp_blend(plan.handle, _ptr(Yout, "Yout", B * tot * C, lat, 16),
-                          _ptr(Z, "Z", B * T * C, lat, 16), _stream(stream)), "tdp_blend")
+    c = _Call("tdp_blend")
+    c.run(_lib.tdp_blend, plan.handle, c.ptr(Yout, "Yout", B * tot * C, lat, 16),
+          c.ptr(Z, "Z", B * T * C, lat, 16), stream=stream)
 
 
 # ------------------------------------------------------------------ allocation helpers

@@ -93,10 +93,12 @@ tdp_cond_blend_kernel(const __grid_constant__ tdp_geom g, int32_t N, int32_t nca
         const bool act = cv < CV;
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // runs before the current one
         float run[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // the current run of kRunRows rows
-        int32_t n = 0;
+        int32_t n = 0;                                       // stored rows summed so far
+        int32_t den = 0;                                     // tiles that kept the token
         for (int32_t t0 = 0; t0 < g.nt; t0 += 32) {
             const int32_t t = t0 + lane;
             const int32_t sl = t < g.nt ? __ldg(slot + ((int64_t)t * g.B + b) * N + k) : -1;
+            den += __popc(__ballot_sync(0xffffffffu, sl >= 0));
             uint32_t m = __ballot_sync(0xffffffffu, sl >= 0 && sl < ncap);
             while (m) {                                      // warp-uniform
                 uint4 y[kRowsInFlight];
@@ -130,7 +132,7 @@ tdp_cond_blend_kernel(const __grid_constant__ tdp_geom g, int32_t N, int32_t nca
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[e] += run[e];
         }
-        if (act) __stcs(out + tok * CV + cv, n > 0 ? acc_div<BF16>(acc, (float)n) : make_uint4(0u, 0u, 0u, 0u));
+        if (act) __stcs(out + tok * CV + cv, den > 0 ? acc_div<BF16>(acc, (float)den) : make_uint4(0u, 0u, 0u, 0u));
     }
 }
 
@@ -140,7 +142,8 @@ tdp_cond_blend_kernel(const __grid_constant__ tdp_geom g, int32_t N, int32_t nca
 //         reused after the lists are built as part [8][P][lpt] float: run sums of a chunk
 //         of P = kPartFloats / (8 lpt) runs
 //   carry [2][8][32] float  sum so far of the token that continues past a chunk (by chunk parity)
-//   len   [kRunTok] int32, run0 [kRunTok + 1] int32  (first run of each token; run0[kRunTok] = runs)
+//   len   [kRunTok] int32 stored rows per token, then den [kRunTok] int32 tiles that kept it
+//   run0  [kRunTok + 1] int32  (first run of each token; run0[kRunTok] = runs)
 //   tab   [kRunTok * ceil(nt / kRunRows)] uint16  run -> (token << 8) | run index within the token
 __host__ __device__ constexpr size_t run_max(size_t a, size_t b) { return a > b ? a : b; }
 
@@ -150,7 +153,7 @@ struct run_layout {
         : slot((size_t)kRunTok * nt * 4),
           carry(slot + run_max((size_t)nt * (kRunTok + 1) * 4, (size_t)kPartFloats * 4)),
           len(carry + 2 * 8 * 32 * 4),
-          run0(len + kRunTok * 4),
+          run0(len + 2 * kRunTok * 4),
           tab(run0 + (kRunTok + 1) * 4),
           bytes((tab + (size_t)kRunTok * ((nt + kRunRows - 1) / kRunRows) * 2 + 15) & ~(size_t)15)
     {
@@ -187,6 +190,7 @@ tdp_cond_blend_runs_kernel(const __grid_constant__ tdp_geom g, int32_t N, int32_
     float *s_part = reinterpret_cast<float *>(dsm + L.slot);
     float *s_carry = reinterpret_cast<float *>(dsm + L.carry);
     int32_t *s_len = reinterpret_cast<int32_t *>(dsm + L.len);
+    int32_t *s_den = s_len + kRunTok;
     int32_t *s_run0 = reinterpret_cast<int32_t *>(dsm + L.run0);
     uint16_t *s_tab = reinterpret_cast<uint16_t *>(dsm + L.tab);
     tdp_pdl_trigger();
@@ -216,16 +220,20 @@ tdp_cond_blend_runs_kernel(const __grid_constant__ tdp_geom g, int32_t N, int32_
     __syncthreads();
     // per token, the rows of the tiles that kept it, in ascending tile order
     for (int32_t j = warp; j < kRunTok; j += kRunThreads / 32) {
-        int32_t len = 0;
+        int32_t len = 0, den = 0;
         for (int32_t t0 = 0; t0 < nt; t0 += 32) {
             const int32_t t = t0 + lane;
             const int32_t sl = t < nt ? s_slot[t * (kRunTok + 1) + j] : -1;
+            den += __popc(__ballot_sync(0xffffffffu, sl >= 0));
             const uint32_t m = __ballot_sync(0xffffffffu, sl >= 0 && sl < ncap);
             if ((m >> lane) & 1u)
                 s_row[j * nt + len + __popc(m & ((1u << lane) - 1u))] = ((uint32_t)t * g.B + b) * (uint32_t)ncap + sl;
             len += __popc(m);
         }
-        if (lane == 0) s_len[j] = k0 + j < N ? len : -1;
+        if (lane == 0) {
+            s_len[j] = k0 + j < N ? len : -1;
+            s_den[j] = den;
+        }
     }
     __syncthreads();
     // runs: a token has max(1, ceil(len / kRunRows)) of them (a token no tile kept has one
@@ -262,13 +270,13 @@ tdp_cond_blend_runs_kernel(const __grid_constant__ tdp_geom g, int32_t N, int32_
             const int32_t c1 = min(U, c0 + P);
             for (int32_t u = c0 + grp; u < c1; u += G) {
                 const uint32_t e = s_tab[u];
-                const int32_t j = (int32_t)(e >> 8), len = s_len[j];
+                const int32_t j = (int32_t)(e >> 8), len = s_len[j], den = s_den[j];
                 float part[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
                 if (act) run_rows<BF16>(s_row + j * nt, Ycond, CV, cv, (int32_t)(e & 255u) * kRunRows, len, part);
                 if (s_run0[j + 1] - s_run0[j] == 1) {
                     if (act)
                         __stcs(out + ((int64_t)b * N + k0 + j) * CV + cv,
-                               len > 0 ? acc_div<BF16>(part, (float)len) : make_uint4(0u, 0u, 0u, 0u));
+                               den > 0 ? acc_div<BF16>(part, (float)den) : make_uint4(0u, 0u, 0u, 0u));
                 } else {
 #pragma unroll
                     for (int x = 0; x < 8; ++x) s_part[(x * P + (u - c0)) * lpt + gl] = part[x];
@@ -289,7 +297,7 @@ tdp_cond_blend_runs_kernel(const __grid_constant__ tdp_geom g, int32_t N, int32_
                     for (int x = 0; x < 8; ++x) acc[x] += s_part[(x * P + (q - c0)) * lpt + gl];
                 }
                 if (re <= c1) {
-                    if (act) __stcs(out + ((int64_t)b * N + k0 + j) * CV + cv, acc_div<BF16>(acc, (float)s_len[j]));
+                    if (act) __stcs(out + ((int64_t)b * N + k0 + j) * CV + cv, acc_div<BF16>(acc, (float)s_den[j]));
                 } else {
                     float *cout = s_carry + (ci & 1) * 256;
 #pragma unroll

@@ -80,8 +80,8 @@ __device__ __forceinline__ void block_sum2(int32_t &x, int32_t &y, int32_t (*s)[
 __global__ void __launch_bounds__(kThreads)
 tdp_compact_kernel(const __grid_constant__ tdp_geom g, const int2 *__restrict__ K, int32_t N, int32_t nchunk,
                    const int32_t *__restrict__ mn, int32_t normalize, const uint8_t *__restrict__ keep,
-                   int32_t *__restrict__ idx, int32_t *__restrict__ count, int2 *__restrict__ Kout,
-                   int32_t *__restrict__ slot)
+                   int32_t vec16, int32_t *__restrict__ idx, int32_t *__restrict__ count,
+                   int2 *__restrict__ Kout, int32_t *__restrict__ slot)
 {
     __shared__ compact_smem sm;
     tdp_pdl_wait();
@@ -93,7 +93,7 @@ tdp_compact_kernel(const __grid_constant__ tdp_geom g, const int2 *__restrict__ 
 
     // ---- kept tokens of (t, b) before this chunk and in all
     int32_t before = 0, total = 0;
-    if ((tb * N) % 16 == 0 && N % 16 == 0) {                     // 16 keep bytes per load
+    if (vec16) {          // keep 16-byte aligned and N % 16 == 0 (checked on the host): 16 bytes per load
         const uint4 *q = reinterpret_cast<const uint4 *>(krow);
         for (int32_t i = threadIdx.x; i < N / 16; i += blockDim.x) {
             const uint4 v = __ldg(q + i);
@@ -159,9 +159,12 @@ extern "C" tdp_status tdp_norm_filter(tdp_plan_t plan, const int32_t *K, int32_t
     if (N > 0)
         err = tdp_launch(true, tdp_keep_kernel, (unsigned)blocks1, kThreads, s, g, k2, N, nchunk, mn, mx, keep,
                          kcount);
+    // every row keep + tb*N is then 16-byte aligned too
+    const int32_t vec16 = N % 16 == 0 && tdp_aligned(keep, 16) ? 1 : 0;
     if (err == cudaSuccess)
         err = tdp_launch(true, tdp_compact_kernel, (unsigned)nkeep, kThreads, s, g, k2, N, nchunk, mn, normalize,
-                         static_cast<const uint8_t *>(keep), idx, count, reinterpret_cast<int2 *>(Kout), slot);
+                         static_cast<const uint8_t *>(keep), vec16, idx, count, reinterpret_cast<int2 *>(Kout),
+                         slot);
     if (err == cudaSuccess) err = cudaGetLastError();
     if (err != cudaSuccess) return tdp_fail(TDP_ERR_CUDA, cudaGetErrorString(err));
     return tdp_ok();

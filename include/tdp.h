@@ -229,14 +229,16 @@ tdp_status tdp_split_filter(tdp_plan_t plan, const void *X, const int32_t *P, co
  *  several times.)
  *
  * out[b,k,:] = (1/n) * sum over the tiles t that kept token k of
- * Ycond[t,b,slot[t,b,k],:], n = number of those tiles; fp32 accumulation in
- * ascending t, in runs of 8 consecutive kept tiles whose sums are added in
- * order, one division per element by n, stored in the plan's dtype.  A token
- * that no tile kept gets 0.
+ * Ycond[t,b,slot[t,b,k],:], n = number of those tiles (slot >= 0, i.e. kcount);
+ * fp32 accumulation in ascending t, in runs of 8 consecutive stored rows whose
+ * sums are added in order, one division per element by n, stored in the plan's
+ * dtype.  A token that no tile kept gets 0.
  *
  *   N      conditioning tokens per batch item (>= 0).
- *   ncap   rows reserved per (tile, batch item) in Ycond (>= 1); slots >= ncap
- *          are ignored, so ncap >= max count keeps every contribution.
+ *   ncap   rows reserved per (tile, batch item) in Ycond (>= 1).  A tile that kept
+ *          the token at slot >= ncap has no stored row: its term is left out of the
+ *          sum while n still counts it, so every stored term keeps the weight 1/n.
+ *          ncap >= max count keeps every contribution.
  *   Ycond  device [n_tiles, B, ncap, C] (plan dtype): row p of (t,b) is the
  *          per-tile transformer's output for the p-th token t kept for item b.
  *   slot   device [n_tiles, B, N] int32 from tdp_norm_filter.

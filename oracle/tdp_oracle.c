@@ -362,8 +362,12 @@ void oracle_blend_cell(const oracle_problem *p, const void *Yout, int32_t b,
  * 1 / (number of tiles that kept it)).  Ycond holds each tile's outputs for its
  * kept conditioning tokens, [nt][B][ncap][C], row p of (t,b) = the p-th kept
  * token.  out[b,k,:] = sum over the tiles t that kept k (ascending) of
- * Ycond[t,b,slot,:] / kcount[b,k], in fp64.
- * Reading taken: a token no tile kept has no tile output; its result is 0.
+ * Ycond[t,b,slot,:] / n, in fp64, with n = the number of tiles that kept k
+ * (kcount[b,k], the page's denominator).
+ * Readings taken: a token no tile kept has no tile output; its result is 0.
+ * Only ncap rows per (t,b) are stored: a tile that kept k at a position p >= ncap
+ * has no stored output for it, so its term is missing from the sum, while the
+ * weight of every stored term stays 1/n.
  * ---------------------------------------------------------------------- */
 void oracle_cond_blend(const oracle_problem *p, int32_t N, int32_t ncap, const void *Ycond,
                        const uint8_t *keep, const int32_t *idx, const int32_t *count, double *out)
@@ -373,20 +377,20 @@ void oracle_cond_blend(const oracle_problem *p, int32_t N, int32_t ncap, const v
         for (int32_t k = 0; k < N; ++k) {
             double *o = out + ((int64_t)b * N + k) * p->C;
             for (int32_t c = 0; c < p->C; ++c) o[c] = 0.0;
-            int32_t kept_by = 0;
+            int32_t n_keep = 0;                      /* tiles that kept k */
             for (int t = 0; t < nt; ++t) {
                 int64_t tb = (int64_t)t * p->B + b;
                 if (!keep[tb * N + k]) continue;
+                n_keep += 1;
                 int32_t pos = -1;                    /* find k in the tile's kept list */
                 for (int32_t q = 0; q < count[tb]; ++q)
                     if (idx[tb * N + q] == k) { pos = q; break; }
-                if (pos < 0 || pos >= ncap) continue;
-                kept_by += 1;
+                if (pos < 0 || pos >= ncap) continue;    /* no stored output row */
                 for (int32_t c = 0; c < p->C; ++c)
                     o[c] += load_elem(Ycond, p->esize, (tb * ncap + pos) * p->C + c);
             }
-            if (kept_by > 0)
-                for (int32_t c = 0; c < p->C; ++c) o[c] /= (double)kept_by;
+            if (n_keep > 0)
+                for (int32_t c = 0; c < p->C; ++c) o[c] /= (double)n_keep;
         }
 }
 

@@ -257,3 +257,31 @@ def test_parity_wide_channels(tdp):
                                     overlap=(0, 2, 2), n_cond=100)
     X, P, K = wk.make_inputs(wl)
     _check_path(tdp, wl, X, P, K)
+
+
+def test_filter_keep_buffer_at_odd_address(tdp):
+    """A keep buffer that starts one byte past a 16-byte boundary, with N a multiple of 16:
+    the compaction reads keep bytes one at a time (its 16-byte loads need an aligned
+    buffer, checked on the host), and every output still matches the oracle."""
+    import torch
+    wl = wk.by_name("small")
+    X, P, K = wk.make_inputs(wl)
+    plan = _plan(tdp, wl)
+    p = oracle.problem_of(wl)
+    N = K.shape[2]
+    assert N % 16 == 0
+    _, Qref = oracle.split(p, X, P)
+    mn, mx = oracle.bounds(p, Qref)
+    ref = dict(zip(("keep", "idx", "count", "kcount", "Kout", "slot"),
+                   oracle.filter_cond(p, K, mn, mx, True, with_slot=True)))
+    nt, B = plan.n_tiles, wl.B
+    raw = torch.full((nt * B * N + 16,), 0xAB, dtype=torch.uint8, device="cuda")
+    keep = raw[1:1 + nt * B * N]
+    assert keep.data_ptr() % 16 == 1
+    _, idx, count, kcount, Kout, slot = tdp.alloc_filter_outputs(plan, N, "cuda", slot=True)
+    tdp.tdp_norm_filter(plan, to_dev(K), N, to_dev(mn), to_dev(mx), 1, keep, idx, count, kcount, Kout, slot)
+    torch.cuda.synchronize()
+    out = dict(keep=to_host(keep).reshape(nt, B, N), idx=to_host(idx), count=to_host(count),
+               kcount=to_host(kcount), Kout=to_host(Kout), slot=to_host(slot))
+    assert_filter_equal(out, ref, nt, B)
+    assert to_host(raw)[0] == 0xAB and (to_host(raw)[1 + nt * B * N:] == 0xAB).all()

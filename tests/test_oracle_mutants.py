@@ -50,10 +50,12 @@ MUTANTS = [
      "return ramp(p, 1, iH, h) * ramp(p, 2, iW, w);"),
     ("bf16_decode_shift", "uint32_t bits = (uint32_t)((const uint16_t *)Y)[i] << 16;",
      "uint32_t bits = (uint32_t)((const uint16_t *)Y)[i] << 15;"),
-    ("cond_divides_by_tiles", "for (int32_t c = 0; c < p->C; ++c) o[c] /= (double)kept_by;",
+    ("cond_divides_by_tiles", "for (int32_t c = 0; c < p->C; ++c) o[c] /= (double)n_keep;",
      "for (int32_t c = 0; c < p->C; ++c) o[c] /= (double)nt;"),
     ("cond_skips_first_tile", "for (int t = 0; t < nt; ++t) {\n                int64_t tb = (int64_t)t * p->B + b;\n                if (!keep",
      "for (int t = 1; t < nt; ++t) {\n                int64_t tb = (int64_t)t * p->B + b;\n                if (!keep"),
+    ("cond_divides_by_stored_rows", "if (pos < 0 || pos >= ncap) continue;",
+     "if (pos < 0 || pos >= ncap) { n_keep -= 1; continue; }"),
     ("mean_off_by_one", "out[i] = acc / (double)nt;", "out[i] = acc / (double)(nt + 1);"),
     ("slot_off_by_one", "slot[tb * N + k] = kept ? cnt : -1;", "slot[tb * N + k] = kept ? cnt + 1 : -1;"),
 ]

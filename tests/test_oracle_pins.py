@@ -516,6 +516,32 @@ def test_cond_blend_single_keeper_is_exact_and_linear():
         assert np.array_equal(oa[bb, k], a[t, bb, slot[t, bb, k]].astype(np.float64))
 
 
+def test_cond_blend_rows_past_capacity_keep_the_page_weight():
+    """Hand-built case with one stored row per (tile, batch item) (ncap = 1), fixed by hand.
+    Four tiles, four tokens; token 3 is kept by every tile but stored only by tile 1 (its
+    only kept token there).  The page's weight is 1/(tiles that kept it) = 1/4, so its
+    output is tile 1's row / 4, not tile 1's row alone; the other tokens have one keeper
+    each and come back whole."""
+    p = oracle.problem(1, 1, 8, 8, 4, 4, (1, 2, 2), (0, 2, 2))      # fp32, C = 4, 4 tiles
+    N, ncap = 4, 1
+    kept = {0: [0, 3], 1: [3], 2: [1, 3], 3: [2, 3]}                  # tile -> kept tokens
+    keep = np.zeros((4, 1, N), np.uint8)
+    idx = np.full((4, 1, N), -1, np.int32)
+    count = np.zeros((4, 1), np.int32)
+    for t, ks in kept.items():
+        keep[t, 0, ks] = 1
+        idx[t, 0, :len(ks)] = ks
+        count[t, 0] = len(ks)
+    base = np.array([1.0, 2.0, 3.0, 4.0], np.float32)
+    Yc = np.stack([(t + 1) * base for t in range(4)]).reshape(4, 1, ncap, 4).astype(np.float32)
+    out = oracle.cond_blend(p, Yc, keep, idx, count, ncap)
+    expect = np.array([[1.0, 2.0, 3.0, 4.0],       # token 0: tile 0 only, row 0
+                       [3.0, 6.0, 9.0, 12.0],      # token 1: tile 2 only, row 0
+                       [4.0, 8.0, 12.0, 16.0],     # token 2: tile 3 only, row 0
+                       [0.5, 1.0, 1.5, 2.0]])      # token 3: 4 keepers, one stored row (tile 1: 2*base) / 4
+    assert np.array_equal(out[0], expect)
+
+
 def test_tile_mean_pins():
     wl = wk.by_name("temporal")
     p = oracle.problem_of(wl.replace(dtype="f32"))
