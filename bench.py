@@ -50,7 +50,6 @@ LAUNCHES_PER_STEP = {
 }
 # ncu DRAM-traffic summaries, one per workload: profiles/dram_traffic_<workload>.txt
 PROFILE_DIR = os.path.join(ROOT, "profiles")
-INSTRUMENT_EVERY = 10        # steps between those timed call by call
 
 
 # ----------------------------------------------------------------------------- bytes
@@ -253,23 +252,266 @@ def oracle_step_time(wl, X, P, K):
     return time.perf_counter() - t, int(count.sum())
 
 
-def cpu_baseline(wl, X, P, K, min_seconds=10.0, max_reps=20):
+def host_cores():
+    """Host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def _oracle_worker(conn, wl):
+    """One oracle process: draws the workload's inputs once, then runs one oracle pass per
+    request and answers with (seconds, kept tokens)."""
+    X, P, K = wk.make_inputs(wl)
+    conn.send("ready")
+    while True:
+        msg = conn.recv()
+        if msg is None:
+            break
+        conn.send(oracle_step_time(wl, X, P, K))
+    conn.close()
+
+
+class OraclePool:
+    """`n` processes (spawn start method: the parent may already hold a CUDA context), each
+    running the oracle as it stands, single-threaded, on its own copy of workload `wl`.  A
+    step sends every process one pass at once and ends when the last one is done, so
+    n passes over the workload take the slowest process's time."""
+
+    def __init__(self, wl, n):
+        import multiprocessing as mp
+        ctx = mp.get_context("spawn")
+        self.n, self.wl = n, wl
+        self.conns, self.procs = [], []
+        for _ in range(n):
+            a, b = ctx.Pipe()
+            pr = ctx.Process(target=_oracle_worker, args=(b, wl), daemon=True)
+            pr.start()
+            self.conns.append(a)
+            self.procs.append(pr)
+        for c in self.conns:
+            assert c.recv() == "ready"
+
+    def step(self):
+        """(wall seconds of one pass on every process, kept tokens of one pass)."""
+        t = time.perf_counter()
+        for c in self.conns:
+            c.send("pass")
+        res = [c.recv() for c in self.conns]
+        return time.perf_counter() - t, res[0][1]
+
+    def close(self):
+        for c in self.conns:
+            try:
+                c.send(None)
+            except OSError:
+                pass
+        for pr in self.procs:
+            pr.join(timeout=30)
+            if pr.is_alive():
+                pr.kill()
+
+
+def oracle_pool(wl_full, seconds_per_step, n):
+    """(OraclePool of `n` processes, the workload each runs): the workload cut to its first
+    frames (same H/W tiling) so that one round -- one pass in every process at once --
+    takes about `seconds_per_step`, sized from a round on an 8-frame probe (the processes
+    share the host's memory bandwidth, so a round is slower than one pass alone)."""
+    import oracle
+    probe = wl_full.replace(F=min(8, wl_full.F))
+    pool = OraclePool(probe, n)
+    try:
+        pool.step()
+        t8 = pool.step()[0]
+    finally:
+        pool.close()
+    Fs = int(min(wl_full.F, max(probe.F, probe.F * int(seconds_per_step / max(t8, 1e-6)))))
+    wl = wl_full
+    if Fs < wl_full.F:
+        try:
+            oracle.plan(oracle.problem_of(wl_full.replace(F=Fs)))     # the tiling must stay valid
+            wl = wl_full.replace(F=Fs)
+        except ValueError:
+            pass
+    return OraclePool(wl, n), wl
+
+
+def sample_words(wl, wl_full):
+    return (f"first {wl.F} of {wl_full.F} frames (same H/W tiling)" if wl.F < wl_full.F
+            else "whole workload")
+
+
+def cpu_baseline(wl, X, P, K, seconds=12.0):
+    """The oracle timed on this host's cores: `host_cores()` processes at once, each on a
+    bounded sample of the workload (its first frames), plus one core on the whole workload."""
     import oracle
     oracle.build()
     box, off = oracle.plan(oracle.problem_of(wl))
+    # one core, whole workload
     times, kept = [], 0
-    while (sum(times) < min_seconds and len(times) < max_reps) or not times:
+    while (sum(times) < seconds / 2 and len(times) < 10) or len(times) < 2:
         dt, kept = oracle_step_time(wl, X, P, K)
         times.append(dt)
-    ab = algorithmic_bytes(wl, int(off[-1]), box.shape[0], kept)["step"]
-    mean = sum(times) / len(times)
-    return {"value": ab / mean / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": (f"whole {wl.name} workload, {len(times)} passes ({sum(times):.1f} s), "
-                       f"single-threaded C oracle, fp64 blend"),
-            "s_per_step": mean}
+    ab1 = algorithmic_bytes(wl, int(off[-1]), box.shape[0], kept)["step"]
+    single = {"value": ab1 / (sum(times) / len(times)) / 1e9, "unit": "GB/s", "cores": 1,
+              "sample": f"whole {wl.name} workload, {len(times)} passes ({sum(times):.1f} s)"}
+    # every core, one sample per process
+    n = host_cores()
+    pool, ws = oracle_pool(wl, 1.0, n)
+    bs, offs = oracle.plan(oracle.problem_of(ws))
+    try:
+        pool.step()                                   # first touch of every process's pages
+        steps, kept_s = [], 0
+        while sum(steps) < seconds / 2 or len(steps) < 2:
+            dt, kept_s = pool.step()
+            steps.append(dt)
+    finally:
+        pool.close()
+    abs_ = algorithmic_bytes(ws, int(offs[-1]), bs.shape[0], kept_s)["step"]
+    mean = sum(steps) / len(steps)
+    return {"value": n * abs_ / mean / 1e9, "unit": "GB/s", "cores": n, "kind": "oracle",
+            "sample": (f"{n} single-threaded oracle processes at once, each on the {wl.name} workload "
+                       f"({sample_words(ws, wl)}); {len(steps)} rounds of one pass in each process "
+                       f"({sum(steps):.1f} s); fp64 blend"),
+            "s_per_round": mean, "single_core": single}
 
 
 # ----------------------------------------------------------------------------- GPU arm
+PER_CALL_REPS = 100          # launches each per-call figure averages
+
+
+class DeviceCase:
+    """One workload resident on the device: inputs, every output buffer, the tile outputs
+    fed to the blend (split tiles + N(0, sigma) noise, made once) and the library calls of
+    the hot path bound to them, all on stream `s`."""
+
+    def __init__(self, tdp, torch, wl, dev, s, X=None, P=None, K=None):
+        self.tdp, self.torch, self.wl, self.s = tdp, torch, wl, s
+        if X is None:
+            X, P, K = wk.make_inputs(wl)
+        self.X, self.P, self.K = X, P, K
+        self.plan = tdp.tdp_plan_create(wl.B, wl.F, wl.H, wl.W, wl.C, wl.dtype, wl.num_tiles, wl.overlap)
+        self.N = K.shape[2]
+        with torch.cuda.stream(s):
+            self.Xd, self.Pd, self.Kd = self.to_dev(X, dev), self.to_dev(P, dev), self.to_dev(K, dev)
+            self.Y, self.Q, self.mn, self.mx = tdp.alloc_split_outputs(self.plan, dev)
+            (self.keep, self.idx, self.count, self.kcount,
+             self.Kout) = tdp.alloc_filter_outputs(self.plan, self.N, dev)
+            self.Z = torch.empty_like(self.Xd)
+            tdp.tdp_pos_bounds(self.plan, self.Pd, self.mn, self.mx, stream=s)
+            tdp.tdp_split(self.plan, self.Xd, self.Pd, self.mn, 1, self.Y, self.Q, stream=s)
+            gen = torch.Generator(device=dev).manual_seed(wl.seed + 7)
+            self.gen = gen
+            noise = wl.sigma * torch.randn(self.Y.shape, generator=gen, device=dev)
+            self.Yout = (self.Y.float() + noise).to(self.Y.dtype)
+            del noise
+        s.synchronize()
+        self.split_filter()
+        s.synchronize()
+        self.kept = int(self.count.sum().item())
+        self.ab = algorithmic_bytes(wl, self.plan.total_tile_tokens, self.plan.n_tiles, self.kept)
+
+    @staticmethod
+    def to_dev(a, dev):
+        import torch
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(a).to(dev)
+
+    # the calls of one step
+    def split_filter(self, X=None, P=None, K=None):
+        self.tdp.tdp_split_filter(self.plan, self.Xd if X is None else X, self.Pd if P is None else P,
+                                  self.Kd if K is None else K, self.N, 1, self.Y, self.Q, self.mn, self.mx,
+                                  self.keep, self.idx, self.count, self.kcount, self.Kout, stream=self.s)
+
+    def pos_bounds(self, P=None):
+        self.tdp.tdp_pos_bounds(self.plan, self.Pd if P is None else P, self.mn, self.mx, stream=self.s)
+
+    def split(self, X=None, P=None):
+        self.tdp.tdp_split(self.plan, self.Xd if X is None else X, self.Pd if P is None else P, self.mn, 1,
+                           self.Y, self.Q, stream=self.s)
+
+    def norm_filter(self, K=None):
+        self.tdp.tdp_norm_filter(self.plan, self.Kd if K is None else K, self.N, self.mn, self.mx, 1, self.keep,
+                                 self.idx, self.count, self.kcount, self.Kout, stream=self.s)
+
+    def blend(self, Z=None):
+        self.tdp.tdp_blend(self.plan, self.Yout, self.Z if Z is None else Z, stream=self.s)
+
+    def pre_model(self, path, X=None, P=None, K=None):
+        if path == "fused":
+            self.split_filter(X, P, K)
+        else:
+            self.pos_bounds(P)
+            self.split(X, P)
+            self.norm_filter(K)
+
+    def step(self, path):
+        self.pre_model(path)
+        self.blend()
+
+    def inputs_fit_l2(self):
+        return self.wl.B * self.plan.total_tile_tokens * self.wl.C * self.wl.esize <= L2_BYTES
+
+
+class L2Flush:
+    """Empties L2 between timed launches: a write of 256 MB (twice L2) and then a read of
+    another 256 MB, so that the next launch starts with its inputs in HBM and no dirty
+    lines of the flush left to write back inside its interval."""
+
+    def __init__(self, torch, dev):
+        self.w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        self.r = torch.ones(256 << 20, dtype=torch.uint8, device=dev)
+
+    def __call__(self):
+        self.w.fill_(1)
+        self.r.sum()
+
+
+def call_ms(torch, s, fn, reps=PER_CALL_REPS, flush=None):
+    """Mean device time of one call of `fn` on stream `s`: `reps` launches, each bracketed by
+    CUDA events on `s` (and, with `flush`, each after an L2 flush).  The GPU is kept busy
+    while the host queues them, so host-side launch work never falls inside an interval."""
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            fn()
+    s.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    with torch.cuda.stream(s):
+        torch.cuda._sleep(int(4e7))
+        for a0, a1 in ev:
+            if flush is not None:
+                flush()
+            a0.record(s)
+            fn()
+            a1.record(s)
+    s.synchronize()
+    return statistics.mean(a0.elapsed_time(a1) for a0, a1 in ev)
+
+
+def call_entry(t_ms, nbytes, peak):
+    gbs = nbytes / (t_ms * 1e-3) / 1e9
+    return {"ms": t_ms, "algorithmic_bytes": nbytes, "GB/s": gbs, "frac": gbs / peak,
+            "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS}
+
+
+def time_calls(case, torch, peak, flush=None, reps=PER_CALL_REPS):
+    """Per-call device times of every call of the hot path on one workload."""
+    ab, s = case.ab, case.s
+    out = {
+        "split_filter": call_entry(call_ms(torch, s, case.split_filter, reps, flush),
+                                   ab["bounds"] + ab["split"] + ab["filter"], peak),
+        "pos_bounds": call_entry(call_ms(torch, s, case.pos_bounds, reps, flush), ab["bounds"], peak),
+        "split": call_entry(call_ms(torch, s, case.split, reps, flush), ab["split"], peak),
+        "norm_filter": call_entry(call_ms(torch, s, case.norm_filter, reps, flush), ab["filter"], peak),
+        "blend": call_entry(call_ms(torch, s, case.blend, reps, flush), ab["blend"], peak),
+    }
+    out["step"] = call_entry(call_ms(torch, s, lambda: case.step("fused"), reps, flush), ab["step"], peak)
+    out["step"]["latent_tokens_per_s"] = case.wl.B * case.wl.tokens / (out["step"]["ms"] * 1e-3)
+    return out
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -285,68 +527,28 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     wl = wk.by_name(args.workload)
     X, P, K = wk.make_inputs(wl)
-    plan = tdp.tdp_plan_create(wl.B, wl.F, wl.H, wl.W, wl.C, wl.dtype, wl.num_tiles, wl.overlap)
-    N = K.shape[2]
     s = torch.cuda.Stream(device=dev)
+    case = DeviceCase(tdp, torch, wl, dev, s, X, P, K)
+    plan, N, gen = case.plan, case.N, case.gen
+    Xd, Pd, Kd, Z, Yout = case.Xd, case.Pd, case.Kd, case.Z, case.Yout
+    mn, mx = case.mn, case.mx
+    path = args.path
+    peak, peak_kind = hbm_peak()
 
-    def to_dev(a):
-        if a.dtype == np.uint16:
-            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
-        return torch.from_numpy(a).to(dev)
-
-    with torch.cuda.stream(s):
-        Xd, Pd, Kd = to_dev(X), to_dev(P), to_dev(K)
-        Y, Q, mn, mx = tdp.alloc_split_outputs(plan, dev)
-        keep, idx, count, kcount, Kout = tdp.alloc_filter_outputs(plan, N, dev)
-        Z = torch.empty_like(Xd)
-        tdp.tdp_pos_bounds(plan, Pd, mn, mx, stream=s)
-        tdp.tdp_split(plan, Xd, Pd, mn, 1, Y, Q, stream=s)
-        gen = torch.Generator(device=dev).manual_seed(wl.seed + 7)
-        Yout = (Y.float() + wl.sigma * torch.randn(Y.shape, generator=gen, device=dev)).to(torch.bfloat16)
-    s.synchronize()
-
-    fused = args.path == "fused"
+    def step():
+        case.step(path)
 
     def pre_model(Xs, Ps, Ks):
         """The pre-model stage (bounds, split, normalisation, filter) on stream s."""
-        if fused:
-            tdp.tdp_split_filter(plan, Xs, Ps, Ks, N, 1, Y, Q, mn, mx, keep, idx, count, kcount, Kout, stream=s)
-        else:
-            tdp.tdp_pos_bounds(plan, Ps, mn, mx, stream=s)
-            tdp.tdp_split(plan, Xs, Ps, mn, 1, Y, Q, stream=s)
-            tdp.tdp_norm_filter(plan, Ks, N, mn, mx, 1, keep, idx, count, kcount, Kout, stream=s)
-
-    def step(evs=None):
-        if evs is not None:
-            evs[0].record(s)
-        if fused:
-            tdp.tdp_split_filter(plan, Xd, Pd, Kd, N, 1, Y, Q, mn, mx, keep, idx, count, kcount, Kout, stream=s)
-        else:
-            tdp.tdp_pos_bounds(plan, Pd, mn, mx, stream=s)
-            if evs is not None:
-                evs[3].record(s)
-            tdp.tdp_split(plan, Xd, Pd, mn, 1, Y, Q, stream=s)
-            if evs is not None:
-                evs[4].record(s)
-            tdp.tdp_norm_filter(plan, Kd, N, mn, mx, 1, keep, idx, count, kcount, Kout, stream=s)
-        if evs is not None:
-            evs[1].record(s)
-        tdp.tdp_blend(plan, Yout, Z, stream=s)
-        if evs is not None:
-            evs[2].record(s)
+        case.pre_model(path, Xs, Ps, Ks)
 
     for _ in range(args.warmup):
         step()
     s.synchronize()
-    kept_total = int(count.sum().item())
-    ab = algorithmic_bytes(wl, plan.total_tile_tokens, plan.n_tiles, kept_total)
+    ab = case.ab
 
-    # ---- timed region: exactly K steps, barrier + synchronize on both sides
-    # Per-call CUDA events on every INSTRUMENT_EVERY-th step only: an event recorded
-    # between two calls ends the programmatic-launch overlap of their kernels, so the
-    # other steps run as a user's would.
-    per = {i: [torch.cuda.Event(enable_timing=True) for _ in range(5)]
-           for i in range(0, args.steps, INSTRUMENT_EVERY)}
+    # ---- timed region: exactly K steps, barrier + synchronize on both sides, no event
+    # between the calls (an event would end the programmatic-launch overlap of the kernels)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(gpu_id_for_smi(torch, local_rank)) if rank == 0 else None
     time.sleep(0.3 if sampler else 0)
@@ -355,8 +557,8 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     t0 = time.time()
     start.record(s)
-    for i in range(args.steps):
-        step(per.get(i))
+    for _ in range(args.steps):
+        step()
     stop.record(s)
     torch.cuda.synchronize()
     t1 = time.time()
@@ -367,15 +569,9 @@ def run_ours(args, rank, world, local_rank):
     ms = start.elapsed_time(stop) / args.steps
     if world > 1:
         ms = max_over_ranks(ms, dev)
-    if fused:
-        k_ms = {"split_filter": statistics.mean(e[0].elapsed_time(e[1]) for e in per.values())}
-    else:
-        k_ms = {
-            "pos_bounds": statistics.mean(e[0].elapsed_time(e[3]) for e in per.values()),
-            "split": statistics.mean(e[3].elapsed_time(e[4]) for e in per.values()),
-            "norm_filter": statistics.mean(e[4].elapsed_time(e[1]) for e in per.values()),
-        }
-    k_ms["blend"] = statistics.mean(e[1].elapsed_time(e[2]) for e in per.values())
+
+    # ---- every call of the hot path timed on its own, after the timed region
+    kern = time_calls(case, torch, peak) if rank == 0 else {}
 
     # ---- the same step captured once in a CUDA graph and replayed (launch overhead
     # of the four calls paid once); reported beside the headline, not instead of it
@@ -419,40 +615,21 @@ def run_ours(args, rank, world, local_rank):
             Ou = torch.empty((wl.B, La), dtype=torch.bfloat16, device=dev)
         s.synchronize()
         extras = {}
-        # these inputs (~70 MB) fit in L2: each timed launch follows a read of 256 MB
-        # (which leaves no dirty lines), so it starts with its inputs in HBM
-        flush = torch.ones(256 << 20, dtype=torch.uint8, device=dev)
+        # these inputs (~70 MB) fit in L2: each timed launch follows an L2 flush
+        flush = L2Flush(torch, dev)
         reps = 50
-
-        def after_flush_ms(fn):
-            for _ in range(5):
-                fn()
-            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
-            with torch.cuda.stream(s):
-                # keep the GPU busy while the host queues every launch, so that no
-                # host-side gap falls between an event and its kernel
-                torch.cuda._sleep(int(3e7))
-                for a0, a1 in ev:
-                    flush.sum()
-                    a0.record(s)
-                    fn()
-                    a1.record(s)
-            s.synchronize()
-            return statistics.mean(a0.elapsed_time(a1) for a0, a1 in ev)
-
         for name, fn, nbytes in (
             ("cond_blend", lambda: tdp.tdp_cond_blend(plan, N, ncap, Yc, slot2, Oc, stream=s),
              kept_rows * wl.C * wl.esize + plan.n_tiles * wl.B * N * 4 + wl.B * N * wl.C * wl.esize),
             ("tile_mean", lambda: tdp.tdp_tile_mean(plan, La, Au, Ou, stream=s),
              (plan.n_tiles + 1) * wl.B * La * wl.esize)):
-            t_ms = after_flush_ms(fn)
-            extras[name] = {"ms": t_ms, "algorithmic_bytes": nbytes, "GB/s": nbytes / (t_ms * 1e-3) / 1e9,
-                            "frac": nbytes / (t_ms * 1e-3) / 1e9 / hbm_peak()[0],
-                            "timing": f"mean of {reps} launches, each after an L2 flush (256 MB read)"}
+            extras[name] = call_entry(call_ms(torch, s, fn, reps, flush), nbytes, peak)
+            extras[name]["timing"] = f"mean of {reps} launches, each after an L2 flush"
         # what the same timing gives a kernel that does almost nothing: the part of each
         # figure above that is launch and ramp, not bytes
         tiny = torch.zeros(8, device=dev)
-        extras["launch_floor_ms"] = after_flush_ms(lambda: tiny.add_(1))
+        extras["launch_floor_ms"] = call_ms(torch, s, lambda: tiny.add_(1), reps, flush)
+        del flush
         extras["cond_blend"]["shape"] = f"{plan.n_tiles} tiles x {ncap} rows x {wl.C} ch, {kept_rows} kept rows"
         extras["tile_mean"]["shape"] = f"{plan.n_tiles} tiles x {AUDIO_TOKENS} audio tokens x {wl.C} ch (synthetic)"
 
@@ -541,24 +718,42 @@ def run_ours(args, rank, world, local_rank):
 
     if rank != 0:
         return None
-    peak, peak_kind = hbm_peak()
-    kern = {}
-    call_bytes = {"pos_bounds": ab["bounds"], "split": ab["split"], "norm_filter": ab["filter"],
-                  "split_filter": ab["bounds"] + ab["split"] + ab["filter"], "blend": ab["blend"]}
     call_name = {"split_filter": "tdp_split_filter", "split": "tdp_split", "blend": "tdp_blend"}
-    for name, t_ms in k_ms.items():
-        b = call_bytes[name]
-        gbs = b / (t_ms * 1e-3) / 1e9
-        kern[name] = {"ms": t_ms, "algorithmic_bytes": b, "GB/s": gbs, "frac": gbs / peak}
-    big = "split_filter" if fused else "split"
-    dom = "blend" if k_ms["blend"] >= k_ms[big] else big
+    big = "split_filter" if path == "fused" else "split"
+    dom = "blend" if kern["blend"]["ms"] >= kern[big]["ms"] else big
     call = call_name[dom]
     roof = {"bound": "hbm", "kernel": call if call != "tdp_split_filter" else
             "tdp_split_filter (tdp_bounds_init_kernel + tdp_bounds_kernel + tdp_split_filter_kernel)",
             "kernels": CALL_KERNELS[call], "achieved": kern[dom]["GB/s"], "peak": peak,
-            "peak_kind": f"{peak_kind} copy bandwidth", "unit": "GB/s", "frac": kern[dom]["GB/s"] / peak,
+            "peak_kind": f"{peak_kind} copy bandwidth", "unit": "GB/s", "frac": kern[dom]["frac"],
             "traffic": profiled_traffic(call, wl.name), "algorithmic_bytes_per_launch": kern[dom]["algorithmic_bytes"],
-            "frac_of_nominal_8tbs": kern[dom]["GB/s"] / NOMINAL_HBM_GBS}
+            "frac_of_nominal_8tbs": kern[dom]["frac_of_nominal_8tbs"],
+            "timing": f"mean of {PER_CALL_REPS} launches of the call, CUDA events on its stream"}
+
+    # ---- every workload: each call timed the same way; inputs that fit in L2 are
+    # flushed out of it before every launch
+    per_workload = None
+    if not args.no_per_workload:
+        per_workload = {}
+        flush = L2Flush(torch, dev)
+        for w in wk.WORKLOADS:
+            if w.name == wl.name:
+                c, fl = case, None
+            else:
+                c = DeviceCase(tdp, torch, w, dev, s)
+                fl = flush if c.wl.B * c.wl.tokens * c.wl.C * c.wl.esize < 2 * L2_BYTES else None
+            calls = kern if c is case else time_calls(c, torch, peak, flush=fl)
+            per_workload[w.name] = {
+                "config": config_of(w, c.plan.total_tile_tokens, c.plan.n_tiles, "single GPU")["workload"],
+                "l2": "flushed before every launch" if fl is not None else "inputs larger than L2; no flush",
+                "calls": {k: {"ms": v["ms"], "GB/s": v["GB/s"], "frac": v["frac"],
+                              "frac_of_nominal_8tbs": v["frac_of_nominal_8tbs"]} for k, v in calls.items()},
+                "latent_tokens_per_s": calls["step"]["latent_tokens_per_s"],
+            }
+            if c is not case:
+                del c
+                torch.cuda.empty_cache()
+        del flush
     value = world * ab["step"] / (ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -570,13 +765,15 @@ def run_ours(args, rank, world, local_rank):
         "frac_of_peak": value / world / peak, "frac_of_nominal_8tbs": value / world / NOMINAL_HBM_GBS,
         "latent_tokens_per_s": world * wl.B * wl.tokens / (ms * 1e-3),
         "step_algorithmic_bytes": ab["step"], "kernels": kern,
-        "kernels_timing": f"CUDA events around each call on every {INSTRUMENT_EVERY}th timed step",
+        "kernels_timing": (f"after the timed region: mean of {PER_CALL_REPS} launches of each call, CUDA events "
+                           f"on its stream around each launch, the GPU kept busy while the host queued them"),
         "roofline": roof,
         "gpu_launches": LAUNCHES_PER_STEP[args.path] * args.steps, "path": args.path,
         "clocks": sampler.summary(t0, t1) if sampler else None,
         "e2e": e2e,
         "extra_kernels": extras,
         "graph_step": graph,
+        "per_workload": per_workload,
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, X, P, K)
@@ -585,37 +782,39 @@ def run_ours(args, rank, world, local_rank):
 
 # ----------------------------------------------------------------------------- reference arm
 def run_reference(args):
-    """The CPU oracle, as it stands, on this host: K timed steps after W warm-ups, each step
-    a bounded sample of the large workload (its first Fs frames, same spatial tiling)."""
+    """The CPU oracle, as it stands, on this host's cores: K timed steps after W warm-ups.
+    A step runs one oracle pass in each of `host_cores()` single-threaded processes at once,
+    each on a bounded sample of the workload (its first frames, same spatial tiling), so
+    that the whole run stays within a few minutes."""
     import oracle
     oracle.build()
     wl_full = wk.by_name(args.workload)
     budget = 150.0 / max(1, args.steps + args.warmup)        # seconds per step
-    probe = wl_full.replace(F=8)
-    Xp, Pp, Kp = wk.make_inputs(probe)
-    t8, _ = oracle_step_time(probe, Xp, Pp, Kp)
-    Fs = int(min(wl_full.F, max(8, 8 * int(budget / max(t8, 1e-6)))))
-    wl = wl_full.replace(F=Fs) if Fs < wl_full.F else wl_full
-    X, P, K = wk.make_inputs(wl)
+    n = host_cores()
+    pool, wl = oracle_pool(wl_full, budget, n)
     box, off = oracle.plan(oracle.problem_of(wl))
     box_full, off_full = oracle.plan(oracle.problem_of(wl_full))
     times, kept = [], 0
-    for _ in range(args.warmup):
-        oracle_step_time(wl, X, P, K)
-    for _ in range(args.steps):
-        dt, kept = oracle_step_time(wl, X, P, K)
-        times.append(dt)
-    ab = algorithmic_bytes(wl, int(off[-1]), box.shape[0], kept)["step"]
+    try:
+        for _ in range(args.warmup):
+            pool.step()
+        for _ in range(args.steps):
+            dt, kept = pool.step()
+            times.append(dt)
+    finally:
+        pool.close()
+    ab = n * algorithmic_bytes(wl, int(off[-1]), box.shape[0], kept)["step"]
     ms = 1e3 * sum(times) / len(times)
     value = ab / (ms * 1e-3) / 1e9
-    sample = (f"{wl.name} workload cut to its first {wl.F} of {wl_full.F} frames (same H/W tiling, "
-              f"2 frame tiles) per step" if wl.F < wl_full.F else f"whole {wl.name} workload per step")
+    sample = (f"{n} single-threaded oracle processes at once, each running one pass over the {wl.name} "
+              f"workload ({sample_words(wl, wl_full)}) per step")
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_of(wl_full, int(off_full[-1]), box_full.shape[0], "host CPU, 1 thread", device=False),
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "config": config_of(wl_full, int(off_full[-1]), box_full.shape[0], f"host CPU, {n} processes",
+                            device=False),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": n, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -632,6 +831,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip the timing of the extra reductions")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
+    ap.add_argument("--no-per-workload", action="store_true", help="skip the per-call timing of every workload")
     ap.add_argument("--path", choices=["fused", "separate"], default="fused",
                     help="pre-model stage as one tdp_split_filter call, or as three calls")
     args = ap.parse_args()
