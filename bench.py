@@ -47,6 +47,7 @@ AUDIO_TOKENS = 2048          # synthetic per-tile audio latent for the tile-mean
 LAUNCHES_PER_STEP = {
     "fused": 4,       # bounds init, bounds, split + filter, blend
     "separate": 6,    # bounds init, bounds, split, keep, compact, blend
+    "tma": 7,         # bounds init, bounds, bulk-tensor split, split positions, keep, compact, blend
 }
 # ncu DRAM-traffic summaries, one per workload: profiles/dram_traffic_<workload>.txt
 PROFILE_DIR = os.path.join(ROOT, "profiles")
@@ -195,6 +196,8 @@ KERNEL_SOURCES = {
     "tdp_blend_kernel": ["tdp_blend.cu"] + _COMMON,
     "tdp_split_kernel": ["tdp_split.cu", "tdp_filter.cuh"] + _COMMON,
     "tdp_split_filter_kernel": ["tdp_split.cu", "tdp_filter.cuh"] + _COMMON,
+    "tdp_split_tma_kernel": ["tdp_split_tma.cu"] + _COMMON,
+    "tdp_split_pos_kernel": ["tdp_split.cu", "tdp_filter.cuh"] + _COMMON,
     "tdp_bounds_init_kernel": ["tdp_bounds.cu"] + _COMMON,
     "tdp_bounds_kernel": ["tdp_bounds.cu"] + _COMMON,
 }
@@ -202,6 +205,7 @@ KERNEL_SOURCES = {
 CALL_KERNELS = {
     "tdp_split_filter": ["tdp_bounds_init_kernel", "tdp_bounds_kernel", "tdp_split_filter_kernel"],
     "tdp_split": ["tdp_split_kernel"],
+    "tdp_split_tma": ["tdp_split_tma_kernel", "tdp_split_pos_kernel"],
     "tdp_blend": ["tdp_blend_kernel"],
 }
 
@@ -432,6 +436,10 @@ class DeviceCase:
         self.tdp.tdp_split(self.plan, self.Xd if X is None else X, self.Pd if P is None else P, self.mn, 1,
                            self.Y, self.Q, stream=self.s)
 
+    def split_tma(self, X=None, P=None):
+        self.tdp.tdp_split_tma(self.plan, self.Xd if X is None else X, self.Pd if P is None else P, self.mn, 1,
+                               self.Y, self.Q, stream=self.s)
+
     def norm_filter(self, K=None):
         self.tdp.tdp_norm_filter(self.plan, self.Kd if K is None else K, self.N, self.mn, self.mx, 1, self.keep,
                                  self.idx, self.count, self.kcount, self.Kout, stream=self.s)
@@ -444,7 +452,7 @@ class DeviceCase:
             self.split_filter(X, P, K)
         else:
             self.pos_bounds(P)
-            self.split(X, P)
+            (self.split_tma if path == "tma" else self.split)(X, P)
             self.norm_filter(K)
 
     def step(self, path):
@@ -504,6 +512,7 @@ def time_calls(case, torch, peak, flush=None, reps=PER_CALL_REPS):
                                    ab["bounds"] + ab["split"] + ab["filter"], peak),
         "pos_bounds": call_entry(call_ms(torch, s, case.pos_bounds, reps, flush), ab["bounds"], peak),
         "split": call_entry(call_ms(torch, s, case.split, reps, flush), ab["split"], peak),
+        "split_tma": call_entry(call_ms(torch, s, case.split_tma, reps, flush), ab["split"], peak),
         "norm_filter": call_entry(call_ms(torch, s, case.norm_filter, reps, flush), ab["filter"], peak),
         "blend": call_entry(call_ms(torch, s, case.blend, reps, flush), ab["blend"], peak),
     }
@@ -718,8 +727,9 @@ def run_ours(args, rank, world, local_rank):
 
     if rank != 0:
         return None
-    call_name = {"split_filter": "tdp_split_filter", "split": "tdp_split", "blend": "tdp_blend"}
-    big = "split_filter" if path == "fused" else "split"
+    call_name = {"split_filter": "tdp_split_filter", "split": "tdp_split", "split_tma": "tdp_split_tma",
+                 "blend": "tdp_blend"}
+    big = {"fused": "split_filter", "separate": "split", "tma": "split_tma"}[path]
     dom = "blend" if kern["blend"]["ms"] >= kern[big]["ms"] else big
     call = call_name[dom]
     roof = {"bound": "hbm", "kernel": call if call != "tdp_split_filter" else
@@ -832,8 +842,9 @@ def main():
     ap.add_argument("--no-extras", action="store_true", help="skip the timing of the extra reductions")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
     ap.add_argument("--no-per-workload", action="store_true", help="skip the per-call timing of every workload")
-    ap.add_argument("--path", choices=["fused", "separate"], default="fused",
-                    help="pre-model stage as one tdp_split_filter call, or as three calls")
+    ap.add_argument("--path", choices=["fused", "separate", "tma"], default="fused",
+                    help="pre-model stage as one tdp_split_filter call, as three calls, or as three calls "
+                         "with the bulk-tensor split (tdp_split_tma)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -26,7 +26,7 @@ import numpy as np
 __all__ = [
     "TDP_OK", "TDP_F32", "TDP_BF16", "TDP_MAX_TILES_PER_DIM", "TdpError",
     "Plan", "tdp_plan_create", "tdp_plan_info", "tdp_plan_destroy",
-    "tdp_pos_bounds", "tdp_split", "tdp_norm_filter", "tdp_split_filter", "tdp_blend", "tdp_cond_blend",
+    "tdp_pos_bounds", "tdp_split", "tdp_split_tma", "tdp_norm_filter", "tdp_split_filter", "tdp_blend", "tdp_cond_blend",
     "tdp_tile_mean",
     "tdp_balanced_tile_split", "tdp_tiles_for_size", "tdp_rank_tiles",
     "tdp_status_str", "tdp_last_error_detail",
@@ -71,6 +71,8 @@ def _load():
     lib.tdp_pos_bounds.restype = ctypes.c_int
     lib.tdp_split.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp]
     lib.tdp_split.restype = ctypes.c_int
+    lib.tdp_split_tma.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp]
+    lib.tdp_split_tma.restype = ctypes.c_int
     lib.tdp_norm_filter.argtypes = [vp, vp, i32, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp]
     lib.tdp_norm_filter.restype = ctypes.c_int
     lib.tdp_split_filter.argtypes = [vp, vp, vp, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
@@ -303,6 +305,23 @@ def tdp_split(plan: Plan, X, P, mn, normalize, Y, Q, stream=None):
           int(bool(normalize)),
           c.ptr(Y, "Y", B * tot * C, lat, 16),
           c.ptr(Q, "Q", B * tot * 6, (torch.int32,), 8), stream=stream)
+
+
+def tdp_split_tma(plan: Plan, X, P, mn, normalize, Y, Q, err=None, stream=None):
+    """tdp_split with the latent moved by bulk-tensor loads and bulk stores (same outputs);
+    `err` (one int32 on the device, or None) is set to 1 if a load timed out."""
+    torch = _torch()
+    B, T, C, nt, tot = plan.B, plan.F * plan.H * plan.W, plan.C, plan.n_tiles, plan.total_tile_tokens
+    lat = _latent_dtypes(plan)
+    c = _Call("tdp_split_tma")
+    c.run(_lib.tdp_split_tma, plan.handle,
+          c.ptr(X, "X", B * T * C, lat, 16),
+          c.ptr(P, "P", B * 3 * T * 2, (torch.int32,), 8),
+          c.ptr(mn, "mn", nt * B * 3, (torch.int32,), 4),
+          int(bool(normalize)),
+          c.ptr(Y, "Y", B * tot * C, lat, 16),
+          c.ptr(Q, "Q", B * tot * 6, (torch.int32,), 8),
+          c.ptr(err, "err", 1, (torch.int32,), 4), stream=stream)
 
 
 def tdp_norm_filter(plan: Plan, K, N, mn, mx, normalize, keep, idx, count, kcount, Kout, slot=None,

@@ -144,6 +144,22 @@ tdp_split_kernel(const __grid_constant__ tdp_geom g, const uint4 *__restrict__ X
     if (P) split_positions(g, r, P, normalize, Q, mn, sm);
 }
 
+// Block = one latent row (b, f, h): positions only.  Launched by tdp_split_tma as a
+// dependent behind the bulk-tensor latent copy, which is a plain launch (it began after
+// all earlier work in the stream completed) and writes neither P, mn nor Q: the
+// positions therefore run beside that copy, and the wait at the end makes this kernel
+// complete only after the copy has, so that later work sees the whole split.
+__global__ void __launch_bounds__(kSplitThreads)
+tdp_split_pos_kernel(const __grid_constant__ tdp_geom g, const int2 *__restrict__ P, int32_t normalize,
+                     int2 *__restrict__ Q, const int32_t *__restrict__ mn)
+{
+    __shared__ split_smem sm;
+    tdp_pdl_trigger();
+    const split_row_id r = split_table(g, blockIdx.x, true, sm);
+    split_positions(g, r, P, normalize, Q, mn, sm);
+    tdp_pdl_wait();
+}
+
 // Blocks [0, fpos): split rows 0..fpos-1; [fpos, fpos + nfilt): filter blocks
 // (tb = t*B + b); [fpos + nfilt, fpos + nfilt + ncount): count blocks; the rest:
 // split rows fpos.. .  Split rows copy their latent before waiting on the bounds
@@ -201,8 +217,18 @@ int32_t resident_split_blocks()
     return v;
 }
 
-tdp_status check_split_args(const tdp_geom &g, const void *X, const int32_t *P, const int32_t *mn,
-                            int32_t normalize, const void *Y, const int32_t *Q)
+}  // namespace
+
+cudaError_t tdp_launch_split_positions(const tdp_geom &g, const int32_t *P, int32_t normalize, int32_t *Q,
+                                       const int32_t *mn, cudaStream_t s)
+{
+    const int64_t rows = (int64_t)g.B * g.F * g.H;
+    return tdp_launch(true, tdp_split_pos_kernel, (unsigned)rows, kSplitThreads, s, g,
+                      reinterpret_cast<const int2 *>(P), normalize, reinterpret_cast<int2 *>(Q), mn);
+}
+
+tdp_status tdp_check_split_args(const tdp_geom &g, const void *X, const int32_t *P, const int32_t *mn,
+                                int32_t normalize, const void *Y, const int32_t *Q)
 {
     if ((P == nullptr) != (Q == nullptr)) return tdp_fail(TDP_ERR_INVALID_ARG, "P and Q must be both set or both NULL");
     if (P && normalize && !mn) return tdp_fail(TDP_ERR_INVALID_ARG, "normalising needs mn");
@@ -215,14 +241,12 @@ tdp_status check_split_args(const tdp_geom &g, const void *X, const int32_t *P, 
     return TDP_OK;
 }
 
-}  // namespace
-
 extern "C" tdp_status tdp_split(tdp_plan_t plan, const void *X, const int32_t *P, const int32_t *mn,
                                 int32_t normalize, void *Y, int32_t *Q, tdp_stream_t stream)
 {
     if (!plan) return tdp_fail(TDP_ERR_INVALID_ARG, "null plan");
     const tdp_geom &g = plan->g;
-    const tdp_status st = check_split_args(g, X, P, mn, normalize, Y, Q);
+    const tdp_status st = tdp_check_split_args(g, X, P, mn, normalize, Y, Q);
     if (st != TDP_OK) return st;
     if (g.B == 0) return tdp_ok();
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -247,7 +271,7 @@ extern "C" tdp_status tdp_split_filter(tdp_plan_t plan, const void *X, const int
     if (g.B == 0) return tdp_ok();
     if (!P || !Q) return tdp_fail(TDP_ERR_INVALID_ARG, "null P or Q");
     if (!mn || !mx) return tdp_fail(TDP_ERR_INVALID_ARG, "null mn or mx");
-    const tdp_status st = check_split_args(g, X, P, mn, normalize, Y, Q);
+    const tdp_status st = tdp_check_split_args(g, X, P, mn, normalize, Y, Q);
     if (st != TDP_OK) return st;
     if (!count) return tdp_fail(TDP_ERR_INVALID_ARG, "null count");
     if (N > 0 && (!K || !keep || !idx || !kcount || !Kout))

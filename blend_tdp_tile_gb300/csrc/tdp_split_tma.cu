@@ -1,0 +1,302 @@
+// tdp_split_tma.cu -- tile split with the latent moved by the Tensor Memory Accelerator
+// ("Tiled Data Parallelism (TDP)", section "What it is": the patchified latent is split
+// into overlapping tiles; "Position normalization" for the positions, which run in
+// tdp_split_pos_kernel beside the copy).
+//
+// A unit of work is one tile-row segment: batch item b, frame f, row h and W-tile iW,
+// i.e. the cells [lo_W, hi_W) of latent row (b, f, h), SW = hi_W - lo_W cells of C
+// channels.  Inside every tile that holds the row (at most 2 F-tiles x 2 H-tiles,
+// "combos") that segment is one contiguous run of SW*C elements of Y.  So a unit is
+//   - one bulk-tensor load (cp.async.bulk.tensor.5d) of the box {C, box_w, 1, 1, 1} at
+//     (0, lo_W, h, f, b) of a tensor map over this GPU's latent [B, F, H, W, C] into a
+//     shared-memory stage, completing on the stage's mbarrier, and
+//   - one bulk store (cp.async.bulk) of SW*C elements from the stage to each combo's
+//     tile row.
+// box_w is the widest W-tile; a narrower tile's box reads a few cells past its right
+// edge (cells of the neighbouring segment, or the map's zero fill past W) that no
+// store uses.  Consecutive units are consecutive W-tiles of one latent row, so the
+// overlap cells two neighbouring segments share are read from HBM once and from L2
+// the second time.
+//
+// One thread per CTA drives a ring of S stages: S - 1 loads run ahead of the unit
+// whose stores it issues, and a stage is reloaded once the stores issued from it have
+// finished reading it (cp.async.bulk.wait_group.read).  Grid: one CTA per SM, units
+// dealt round-robin, so the CTAs move through the units in order together.  Every
+// mbarrier wait has an iteration limit; past it the CTA records the failure in `err`,
+// stops issuing, waits (again with a limit) for the loads it has in flight and for its
+// stores, and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "tdp.h"
+#include "tdp_device.cuh"
+#include "tdp_internal.h"
+
+namespace {
+
+constexpr int kTmaThreads = 32;                    // one warp; lane 0 drives the pipeline
+constexpr int kTmaMaxStages = 32;
+constexpr uint32_t kTmaSmemBudget = 200u * 1024u;  // dynamic shared memory of a CTA
+constexpr uint32_t kTmaMaxBox = 256;               // tensor-map box extent limit
+constexpr uint32_t kWaitRounds = 1u << 22;         // try_wait rounds before a load counts as lost
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Wait for phase `parity` of the mbarrier at `bar`; false after kWaitRounds attempts.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+{
+    for (uint32_t i = 0; i < kWaitRounds; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+__device__ __forceinline__ void tma_load_box(uint32_t dst, const CUtensorMap *map, uint32_t bar, int32_t c0,
+                                             int32_t c1, int32_t c2, int32_t c3, int32_t c4)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_store(void *gdst, uint32_t src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(src), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// All but the most recent group of bulk stores have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all_but_one()
+{
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
+// Every bulk store of this thread is complete.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Tiles covering x along one dimension: first and (or -1) second.
+__device__ __forceinline__ void cover2(const tdp_dim_geom &dg, int32_t x, int32_t &i0, int32_t &i1)
+{
+    const int32_t ci = (int32_t)(((uint32_t)(x + 1) * (uint32_t)dg.n + (uint32_t)(dg.L - 1)) / (uint32_t)dg.L) - 1;
+    if (ci > 0 && x < dg.hi[ci - 1]) {
+        i0 = ci - 1;
+        i1 = ci;
+    } else if (ci < dg.n - 1 && x >= dg.lo[ci + 1]) {
+        i0 = ci;
+        i1 = ci + 1;
+    } else {
+        i0 = ci;
+        i1 = -1;
+    }
+}
+
+struct unit_id {
+    int32_t b, f, h, iW;
+};
+
+__device__ __forceinline__ unit_id unit_of(const tdp_geom &g, int64_t u)
+{
+    unit_id id;
+    const int32_t nW = g.d[2].n;
+    id.iW = (int32_t)(u % nW);
+    int64_t r = u / nW;
+    id.h = (int32_t)(r % g.H);
+    r /= g.H;
+    id.f = (int32_t)(r % g.F);
+    id.b = (int32_t)(r / g.F);
+    return id;
+}
+
+__global__ void __launch_bounds__(kTmaThreads, 1)
+tdp_split_tma_kernel(const __grid_constant__ CUtensorMap map, const __grid_constant__ tdp_geom g, int64_t n_units,
+                     int32_t stages, uint32_t stage_stride, uint32_t box_bytes, char *__restrict__ Y,
+                     int32_t *__restrict__ err)
+{
+    extern __shared__ __align__(128) unsigned char dsm[];
+    tdp_pdl_trigger();                     // the positions kernel may start beside this one
+    if (threadIdx.x != 0) return;
+    const uint32_t stage0 = smem_addr(dsm);
+    const uint32_t bar0 = stage0 + (uint32_t)stages * stage_stride;   // stages * 8 bytes of mbarriers
+    for (int32_t s = 0; s < stages; ++s) mbar_init(bar0 + 8u * s);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+
+    const int64_t n_mine = n_units > blockIdx.x ? (n_units - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const uint32_t row_bytes = (uint32_t)g.C * (uint32_t)g.esize;
+    const tdp_dim_geom &dW = g.d[2];
+
+    auto issue_load = [&](int64_t i) {
+        const unit_id id = unit_of(g, blockIdx.x + i * (int64_t)gridDim.x);
+        const int32_t s = (int32_t)(i % stages);
+        const uint32_t bar = bar0 + 8u * s;
+        mbar_expect_tx(bar, box_bytes);
+        tma_load_box(stage0 + (uint32_t)s * stage_stride, &map, bar, 0, dW.lo[id.iW], id.h, id.f, id.b);
+    };
+
+    const int64_t pre = n_mine < stages ? n_mine : stages;
+    for (int64_t i = 0; i < pre; ++i) issue_load(i);
+    int64_t issued = pre;                     // loads issued so far (units 0 .. issued-1)
+    int64_t lost_at = -1;                     // unit whose load did not complete in time
+    for (int64_t i = 0; i < n_mine; ++i) {
+        const int32_t s = (int32_t)(i % stages);
+        if (!mbar_wait(bar0 + 8u * s, (uint32_t)((i / stages) & 1))) {
+            lost_at = i;
+            break;
+        }
+        // stores of unit i: one per (F, H) combo holding its row
+        const unit_id id = unit_of(g, blockIdx.x + i * (int64_t)gridDim.x);
+        int32_t f0, f1, h0, h1;
+        cover2(g.d[0], id.f, f0, f1);
+        cover2(g.d[1], id.h, h0, h1);
+        const int32_t SW = dW.hi[id.iW] - dW.lo[id.iW];
+        const uint32_t src = stage0 + (uint32_t)s * stage_stride;
+        for (int32_t a = 0; a < 2; ++a) {
+            const int32_t iF = a ? f1 : f0;
+            if (iF < 0) break;
+            for (int32_t e = 0; e < 2; ++e) {
+                const int32_t iH = e ? h1 : h0;
+                if (iH < 0) break;
+                const int64_t SF = g.d[0].hi[iF] - g.d[0].lo[iF];
+                const int64_t SH = g.d[1].hi[iH] - g.d[1].lo[iH];
+                const int64_t Tt = SF * SH * SW;
+                const int64_t tok = (int64_t)g.B * tdp_tile_off(g, iF, iH, id.iW) + (int64_t)id.b * Tt +
+                                    ((int64_t)(id.f - g.d[0].lo[iF]) * SH + (id.h - g.d[1].lo[iH])) * SW;
+                bulk_store(Y + tok * row_bytes, src, (uint32_t)SW * row_bytes);
+            }
+        }
+        bulk_commit();
+        // refill the stage of unit i - 1, whose stores were committed one unit ago
+        if (i >= 1 && issued < n_mine) {
+            bulk_wait_read_all_but_one();
+            issue_load(issued);
+            ++issued;
+        }
+    }
+    if (lost_at >= 0) {
+        if (err) atomicExch(err, 1);
+        // let the loads still in flight (units lost_at .. issued - 1, at most one per
+        // stage) land before the CTA's shared memory is released
+        for (int64_t j = lost_at; j < issued; ++j) {
+            const int32_t s = (int32_t)(j % stages);
+            mbar_wait(bar0 + 8u * s, (uint32_t)((j / stages) & 1));
+        }
+    }
+    bulk_wait_all();
+}
+
+// cuTensorMapEncodeTiled from the driver, looked up once per process.
+PFN_cuTensorMapEncodeTiled_v12000 encode_tiled()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// CTAs resident per device at the given dynamic shared memory: one per SM.
+int32_t tma_grid(size_t smem)
+{
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    if (cudaFuncSetAttribute(tdp_split_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return sms;
+}
+
+}  // namespace
+
+extern "C" tdp_status tdp_split_tma(tdp_plan_t plan, const void *X, const int32_t *P, const int32_t *mn,
+                                    int32_t normalize, void *Y, int32_t *Q, int32_t *err, tdp_stream_t stream)
+{
+    if (!plan) return tdp_fail(TDP_ERR_INVALID_ARG, "null plan");
+    const tdp_geom &g = plan->g;
+    const tdp_status st = tdp_check_split_args(g, X, P, mn, normalize, Y, Q);
+    if (st != TDP_OK) return st;
+    if (err && !tdp_aligned(err, 4)) return tdp_fail(TDP_ERR_MISALIGNED, "err must be 4-byte aligned");
+    if (g.B == 0) return tdp_ok();
+    int32_t box_w = 0;
+    for (int32_t i = 0; i < g.d[2].n; ++i) box_w = g.d[2].hi[i] - g.d[2].lo[i] > box_w ? g.d[2].hi[i] - g.d[2].lo[i] : box_w;
+    const uint32_t box_bytes = (uint32_t)g.C * (uint32_t)box_w * (uint32_t)g.esize;
+    const uint32_t stage_stride = (box_bytes + 127u) & ~127u;      // stages start 128-byte aligned
+    if ((uint32_t)g.C > kTmaMaxBox || (uint32_t)box_w > kTmaMaxBox || 2 * (stage_stride + 8) > kTmaSmemBudget)
+        return tdp_fail(TDP_ERR_TOO_LARGE,
+                        "tdp_split_tma needs C <= 256, W-tiles at most 256 cells and two boxes of the widest "
+                        "W-tile within 200 KB (tdp_split takes every shape)");
+    PFN_cuTensorMapEncodeTiled_v12000 encode = encode_tiled();
+    if (!encode) return tdp_fail(TDP_ERR_CUDA, "cuTensorMapEncodeTiled not available from the driver");
+
+    CUtensorMap map;
+    const cuuint64_t dims[5] = {(cuuint64_t)g.C, (cuuint64_t)g.W, (cuuint64_t)g.H, (cuuint64_t)g.F, (cuuint64_t)g.B};
+    const cuuint64_t e = (cuuint64_t)g.esize;
+    const cuuint64_t strides[4] = {e * g.C, e * g.C * g.W, e * g.C * g.W * g.H, e * g.C * g.W * g.H * g.F};
+    const cuuint32_t box[5] = {(cuuint32_t)g.C, (cuuint32_t)box_w, 1, 1, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    const CUresult cr = encode(&map, g.dtype == TDP_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                               5, const_cast<void *>(X), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS) return tdp_fail(TDP_ERR_CUDA, "cuTensorMapEncodeTiled rejected the latent's tensor map");
+
+    int32_t stages = (int32_t)(kTmaSmemBudget / (stage_stride + 8));
+    stages = stages > kTmaMaxStages ? kTmaMaxStages : stages;
+    const size_t smem = (size_t)stages * (stage_stride + 8);
+    const int32_t ctas = tma_grid(smem);
+    if (ctas <= 0) return tdp_fail(TDP_ERR_CUDA, "could not size the bulk-tensor split's grid");
+    const int64_t n_units = (int64_t)g.B * g.F * g.H * g.d[2].n;
+    const unsigned grid = (unsigned)(n_units < ctas ? n_units : ctas);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // plain launch: the copy starts once all earlier work in the stream has completed
+    cudaError_t ce = tdp_launch_smem(false, tdp_split_tma_kernel, grid, kTmaThreads, smem, s, map, g, n_units,
+                                     stages, stage_stride, box_bytes, static_cast<char *>(Y), err);
+    if (ce == cudaSuccess && P) ce = tdp_launch_split_positions(g, P, normalize, Q, mn, s);
+    if (ce == cudaSuccess) ce = cudaGetLastError();
+    if (ce != cudaSuccess) return tdp_fail(TDP_ERR_CUDA, cudaGetErrorString(ce));
+    return tdp_ok();
+}

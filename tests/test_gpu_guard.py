@@ -8,8 +8,8 @@ guard band of GUARD bytes on each side:
   that read past an input and used what it found would change a result, and the
   element-by-element comparison with the CPU oracle would fail.
 
-Each case runs every entry point: tdp_pos_bounds, tdp_split, tdp_norm_filter,
-tdp_split_filter, tdp_blend, tdp_cond_blend and tdp_tile_mean, on ragged
+Each case runs every entry point: tdp_pos_bounds, tdp_split, tdp_split_tma,
+tdp_norm_filter, tdp_split_filter, tdp_blend, tdp_cond_blend and tdp_tile_mean, on ragged
 geometries (tails in every dimension, several batch items, minimal and odd
 channel counts).  Method: "Tiled Data Parallelism (TDP)" (LTX-2 docs, multigpu).
 """
@@ -137,6 +137,17 @@ def test_guard_bands(tdp, name, wl):
                          o["idx"].t, o["count"].t, o["kcount"].t, o["Kout"].t, o["slot"].t)
     torch.cuda.synchronize()
     check_split(o, "tdp_split_filter")
+
+    # the latent moved by bulk-tensor loads and bulk stores (positions beside it)
+    o = dict(Y=_output((B * tot, C), lat), Q=_output((B * tot * 6,), i32), err=_output((1,), i32))
+    o["err"].t.zero_()
+    mn_in = _input(mnr)
+    tdp.tdp_split_tma(plan, Xg.t, Pg.t, mn_in.t, 1, o["Y"].t, o["Q"].t, o["err"].t)
+    torch.cuda.synchronize()
+    _check_bands(o, "tdp_split_tma")
+    assert int(o["err"].t.item()) == 0, "tdp_split_tma: a bulk-tensor load timed out"
+    assert np.array_equal(_host(o["Y"]).reshape(Yref.shape), Yref), "tdp_split_tma"
+    assert np.array_equal(_host(o["Q"]), Qn), "tdp_split_tma"
 
     # blend of perturbed tile outputs
     noise = wk.make_noise(Yref.shape, wl.sigma, np.random.default_rng(wl.seed + 7))

@@ -9,7 +9,7 @@ import pytest
 
 import oracle
 import workloads as wk
-from gpu_path import (as_f64, assert_blend_close, assert_filter_equal, run_blend,
+from gpu_path import (as_f64, assert_blend_close, assert_filter_equal, fill_sentinel, run_blend,
                       run_split_filter, to_dev, to_host)
 
 pytestmark = pytest.mark.gpu
@@ -282,3 +282,49 @@ def test_filter_keep_buffer_at_odd_address(tdp):
                kcount=to_host(kcount), Kout=to_host(Kout), slot=to_host(slot))
     assert_filter_equal(out, ref, nt, B)
     assert to_host(raw)[0] == 0xAB and (to_host(raw)[1 + nt * B * N:] == 0xAB).all()
+
+
+@pytest.mark.parametrize("name", FULL_ORACLE + ["large"])
+@pytest.mark.parametrize("normalize", [True, False])
+def test_split_tma_parity(tdp, name, normalize):
+    """tdp_split_tma (bulk-tensor loads of tile-row segments, bulk stores to every tile
+    holding them, positions beside the copy) gives tdp_split's outputs bit for bit."""
+    import torch
+    wl = wk.by_name(name)
+    X, P, K = wk.make_inputs(wl)
+    plan = _plan(tdp, wl)
+    p = oracle.problem_of(wl)
+    Yref, Qref = oracle.split(p, X, P)
+    mn, _ = oracle.bounds(p, Qref)
+    Qexp = oracle.normalize(p, Qref, mn) if normalize else Qref
+    Y, Q, _, _ = tdp.alloc_split_outputs(plan, "cuda")
+    for t in (Y, Q):
+        fill_sentinel(t)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(2):                     # twice: the second call runs over the first's outputs
+        tdp.tdp_split_tma(plan, to_dev(X), to_dev(P), to_dev(mn), int(normalize), Y, Q, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert np.array_equal(to_host(Y).reshape(Yref.shape), Yref)
+    assert np.array_equal(to_host(Q), Qexp)
+
+
+def test_split_tma_without_positions_and_refusals(tdp):
+    """Latent only (P = Q = NULL); and shapes past the tensor-map box limits are refused on
+    the host with TDP_ERR_TOO_LARGE before any launch."""
+    import torch
+    wl = wk.by_name("medium")
+    X, P, _ = wk.make_inputs(wl)
+    plan = _plan(tdp, wl)
+    Y, _, _, _ = tdp.alloc_split_outputs(plan, "cuda", positions=False)
+    fill_sentinel(Y)
+    tdp.tdp_split_tma(plan, to_dev(X), None, None, 1, Y, None)
+    torch.cuda.synchronize()
+    Yref, _ = oracle.split(oracle.problem_of(wl), X, P)
+    assert np.array_equal(to_host(Y).reshape(Yref.shape), Yref)
+    wide = wk.by_name("tiny").replace(F=2, H=3, W=40, C=512, dtype="bf16", num_tiles=(1, 1, 2), overlap=(0, 0, 2))
+    pw = _plan(tdp, wide)
+    Xw = torch.zeros((1, 2, 3, 40, 512), dtype=torch.bfloat16, device="cuda")
+    Yw, _, _, _ = tdp.alloc_split_outputs(pw, "cuda", positions=False)
+    with pytest.raises(tdp.TdpError, match="TDP_ERR_TOO_LARGE"):
+        tdp.tdp_split_tma(pw, Xw, None, None, 1, Yw, None)
