@@ -49,6 +49,7 @@ LAUNCHES_PER_STEP = {
     "separate": 6,    # bounds init, bounds, split, keep, compact, blend
     "tma": 7,         # bounds init, bounds, bulk-tensor split, split positions, keep, compact, blend
 }
+# --parallel round_robin replaces the blend by tdp_blend_partial + tdp_blend_store (one more)
 # ncu DRAM-traffic summaries, one per workload: profiles/dram_traffic_<workload>.txt
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 
@@ -444,8 +445,13 @@ class DeviceCase:
         self.tdp.tdp_norm_filter(self.plan, self.Kd if K is None else K, self.N, self.mn, self.mx, 1, self.keep,
                                  self.idx, self.count, self.kcount, self.Kout, stream=self.s)
 
+    blend_impl = None        # replaces tdp_blend when set (the round-robin ranks' blend)
+
     def blend(self, Z=None):
-        self.tdp.tdp_blend(self.plan, self.Yout, self.Z if Z is None else Z, stream=self.s)
+        if self.blend_impl is not None:
+            self.blend_impl(self.Z if Z is None else Z)
+        else:
+            self.tdp.tdp_blend(self.plan, self.Yout, self.Z if Z is None else Z, stream=self.s)
 
     def pre_model(self, path, X=None, P=None, K=None):
         if path == "fused":
@@ -543,6 +549,14 @@ def run_ours(args, rank, world, local_rank):
     mn, mx = case.mn, case.mx
     path = args.path
     peak, peak_kind = hbm_peak()
+    rr = args.parallel == "round_robin"
+    if rr:
+        # every rank splits the whole latent and holds every tile's output (the stand-in
+        # model); the blend reads only this rank's tiles and the collective sums the ranks
+        from blend_tdp_tile_gb300 import ranks
+        Zp = torch.empty(Z.shape, dtype=torch.float32, device=dev)
+        case.blend_impl = lambda Zout: ranks.blend_across_ranks(plan, Yout, Zout, mode=args.collective, Zp=Zp,
+                                                                stream=s)
 
     def step():
         case.step(path)
@@ -580,12 +594,12 @@ def run_ours(args, rank, world, local_rank):
         ms = max_over_ranks(ms, dev)
 
     # ---- every call of the hot path timed on its own, after the timed region
-    kern = time_calls(case, torch, peak) if rank == 0 else {}
+    kern = time_calls(case, torch, peak) if rank == 0 or rr else {}
 
     # ---- the same step captured once in a CUDA graph and replayed (launch overhead
     # of the four calls paid once); reported beside the headline, not instead of it
     graph = None
-    if rank == 0 and not args.no_graph:
+    if rank == 0 and not args.no_graph and not rr:
         with torch.cuda.stream(s):
             step()
         s.synchronize()
@@ -678,7 +692,7 @@ def run_ours(args, rank, world, local_rank):
             s.wait_event(out_free[j])
             pre_model(Xb[j], Pb[j], Kb[j])
             in_free[j].record(s)
-            tdp.tdp_blend(plan, Yout, Zb[j], stream=s)
+            case.blend(Zb[j])
             out_ready[j].record(s)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(out_ready[j])
@@ -719,7 +733,7 @@ def run_ours(args, rank, world, local_rank):
         if world > 1:
             e2e_ms = max_over_ranks(e2e_ms, dev)
         h2d, d2h = X.nbytes + P.nbytes + K.nbytes, X.nbytes
-        e2e = {"value": world * ab["step"] / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+        e2e = {"value": (1 if rr else world) * ab["step"] / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_ms, "steps": args.e2e_steps,
                "copy_floor_ms_per_step": floor_ms, "copy_floor_GBps": (h2d + d2h) / (floor_ms * 1e-3) / 1e9,
@@ -743,7 +757,7 @@ def run_ours(args, rank, world, local_rank):
     # ---- every workload: each call timed the same way; inputs that fit in L2 are
     # flushed out of it before every launch
     per_workload = None
-    if not args.no_per_workload:
+    if not args.no_per_workload and not rr:
         per_workload = {}
         flush = L2Flush(torch, dev)
         for w in wk.WORKLOADS:
@@ -764,21 +778,27 @@ def run_ours(args, rank, world, local_rank):
                 del c
                 torch.cuda.empty_cache()
         del flush
-    value = world * ab["step"] / (ms * 1e-3) / 1e9
+    problems = 1 if rr else world           # round-robin: one problem over all ranks
+    value = problems * ab["step"] / (ms * 1e-3) / 1e9
+    if rr:
+        parallelism = f"round-robin tiles over {world} rank(s), {args.collective} of fp32 partials"
+    else:
+        parallelism = f"replicas x{world}" if world > 1 else "single GPU"
+    launches = LAUNCHES_PER_STEP[args.path] + (1 if rr else 0)       # partial blend + store for the blend
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "strong" if rr else "weak",
         "vs_baseline": None, "dtype": "bf16",
         "dtype_detail": "bf16 latent storage, fp32 blend accumulation, int32 positions",
-        "data": "synthetic", "config": config_of(wl, plan.total_tile_tokens, plan.n_tiles,
-                                                 f"replicas x{world}" if world > 1 else "single GPU"),
+        "data": "synthetic", "config": config_of(wl, plan.total_tile_tokens, plan.n_tiles, parallelism),
         "frac_of_peak": value / world / peak, "frac_of_nominal_8tbs": value / world / NOMINAL_HBM_GBS,
-        "latent_tokens_per_s": world * wl.B * wl.tokens / (ms * 1e-3),
+        "latent_tokens_per_s": problems * wl.B * wl.tokens / (ms * 1e-3),
         "step_algorithmic_bytes": ab["step"], "kernels": kern,
         "kernels_timing": (f"after the timed region: mean of {PER_CALL_REPS} launches of each call, CUDA events "
                            f"on its stream around each launch, the GPU kept busy while the host queued them"),
         "roofline": roof,
-        "gpu_launches": LAUNCHES_PER_STEP[args.path] * args.steps, "path": args.path,
+        "gpu_launches": launches * args.steps, "path": args.path,
         "clocks": sampler.summary(t0, t1) if sampler else None,
         "e2e": e2e,
         "extra_kernels": extras,
@@ -842,6 +862,12 @@ def main():
     ap.add_argument("--no-extras", action="store_true", help="skip the timing of the extra reductions")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
     ap.add_argument("--no-per-workload", action="store_true", help="skip the per-call timing of every workload")
+    ap.add_argument("--parallel", choices=["replicas", "round_robin"], default="replicas",
+                    help="replicas: every rank runs the whole step on its own problem (weak scaling); "
+                         "round_robin: the ranks share one problem, tile t blended on rank t %% N and the "
+                         "partials summed by a collective (strong scaling)")
+    ap.add_argument("--collective", choices=["reduce_scatter", "all_reduce"], default="reduce_scatter",
+                    help="collective of the round_robin blend")
     ap.add_argument("--path", choices=["fused", "separate", "tma"], default="fused",
                     help="pre-model stage as one tdp_split_filter call, as three calls, or as three calls "
                          "with the bulk-tensor split (tdp_split_tma)")
@@ -858,15 +884,22 @@ def main():
             print(json.dumps(run_reference(args)), flush=True)
         return
 
-    if world > 1:
+    distributed = world > 1 or args.parallel == "round_robin"
+    if distributed:
         import torch
         import torch.distributed as dist
+        if "MASTER_ADDR" not in os.environ:          # one rank started without torchrun
+            import socket
+            with socket.socket() as sk:
+                sk.bind(("127.0.0.1", 0))
+                port = sk.getsockname()[1]
+            os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK="0", WORLD_SIZE="1")
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     line = run_ours(args, rank, world, local_rank)
     if rank == 0:
         print(json.dumps(line), flush=True)
-    if world > 1:
+    if distributed:
         import torch.distributed as dist
         dist.barrier()
         dist.destroy_process_group()

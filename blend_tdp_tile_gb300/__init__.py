@@ -27,7 +27,7 @@ __all__ = [
     "TDP_OK", "TDP_F32", "TDP_BF16", "TDP_MAX_TILES_PER_DIM", "TdpError",
     "Plan", "tdp_plan_create", "tdp_plan_info", "tdp_plan_destroy",
     "tdp_pos_bounds", "tdp_split", "tdp_split_tma", "tdp_norm_filter", "tdp_split_filter", "tdp_blend", "tdp_cond_blend",
-    "tdp_tile_mean",
+    "tdp_tile_mean", "tdp_blend_partial", "tdp_blend_store",
     "tdp_balanced_tile_split", "tdp_tiles_for_size", "tdp_rank_tiles",
     "tdp_status_str", "tdp_last_error_detail",
     "alloc_split_outputs", "alloc_filter_outputs", "LIB_PATH",
@@ -83,6 +83,10 @@ def _load():
     lib.tdp_tile_mean.restype = ctypes.c_int
     lib.tdp_blend.argtypes = [vp, vp, vp, vp]
     lib.tdp_blend.restype = ctypes.c_int
+    lib.tdp_blend_partial.argtypes = [vp, i32, i32, vp, vp, vp]
+    lib.tdp_blend_partial.restype = ctypes.c_int
+    lib.tdp_blend_store.argtypes = [vp, ctypes.c_int64, vp, vp, vp]
+    lib.tdp_blend_store.restype = ctypes.c_int
     lib.tdp_balanced_tile_split.argtypes = [i32, ctypes.POINTER(i32), ctypes.POINTER(i32)]
     lib.tdp_balanced_tile_split.restype = ctypes.c_int
     lib.tdp_tiles_for_size.argtypes = [i32, i32, i32, ctypes.POINTER(i32)]
@@ -402,6 +406,28 @@ def tdp_blend(plan: Plan, Yout, Z, stream=None):
     c = _Call("tdp_blend")
     c.run(_lib.tdp_blend, plan.handle, c.ptr(Yout, "Yout", B * tot * C, lat, 16),
           c.ptr(Z, "Z", B * T * C, lat, 16), stream=stream)
+
+
+def tdp_blend_partial(plan: Plan, rank, world, Yout, Zp, stream=None):
+    """Rank `rank` of `world`'s share of the blend (its round-robin tiles t % world == rank)
+    into the fp32 partial latent Zp [B,F,H,W,C]."""
+    torch = _torch()
+    B, T, C, tot = plan.B, plan.F * plan.H * plan.W, plan.C, plan.total_tile_tokens
+    lat = _latent_dtypes(plan)
+    c = _Call("tdp_blend_partial")
+    c.run(_lib.tdp_blend_partial, plan.handle, int(rank), int(world), c.ptr(Yout, "Yout", B * tot * C, lat, 16),
+          c.ptr(Zp, "Zp", B * T * C, (torch.float32,), 16), stream=stream)
+
+
+def tdp_blend_store(plan: Plan, Zsum, Z, stream=None):
+    """Z = Zsum (fp32) in the plan's dtype; Zsum and Z have the same number of elements (the
+    whole latent or a run of whole rows)."""
+    torch = _torch()
+    n = int(Zsum.numel())
+    lat = _latent_dtypes(plan)
+    c = _Call("tdp_blend_store")
+    c.run(_lib.tdp_blend_store, plan.handle, n, c.ptr(Zsum, "Zsum", n, (torch.float32,), 16),
+          c.ptr(Z, "Z", n, lat, 16), stream=stream)
 
 
 # ------------------------------------------------------------------ allocation helpers

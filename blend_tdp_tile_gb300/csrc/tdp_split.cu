@@ -220,10 +220,10 @@ int32_t resident_split_blocks()
 }  // namespace
 
 cudaError_t tdp_launch_split_positions(const tdp_geom &g, const int32_t *P, int32_t normalize, int32_t *Q,
-                                       const int32_t *mn, cudaStream_t s)
+                                       const int32_t *mn, cudaStream_t s, bool pdl)
 {
     const int64_t rows = (int64_t)g.B * g.F * g.H;
-    return tdp_launch(true, tdp_split_pos_kernel, (unsigned)rows, kSplitThreads, s, g,
+    return tdp_launch(pdl, tdp_split_pos_kernel, (unsigned)rows, kSplitThreads, s, g,
                       reinterpret_cast<const int2 *>(P), normalize, reinterpret_cast<int2 *>(Q), mn);
 }
 

@@ -18,10 +18,13 @@
 // overlap cells two neighbouring segments share are read from HBM once and from L2
 // the second time.
 //
-// One thread per CTA drives a ring of S stages: S - 1 loads run ahead of the unit
-// whose stores it issues, and a stage is reloaded once the stores issued from it have
-// finished reading it (cp.async.bulk.wait_group.read).  Grid: one CTA per SM, units
-// dealt round-robin, so the CTAs move through the units in order together.  Every
+// One thread per CTA drives a ring of S stages: the bulk stores of the last PEND units
+// stay in flight (PEND = 4, 2 or 1 by ring depth), the other S - PEND stages hold loads
+// running ahead, and a stage is reloaded once the stores issued from it have finished
+// reading it (cp.async.bulk.wait_group.read).  One CTA's ring moves about 30 GB/s, so
+// an SM holds several: 3 CTAs with 66 KB rings when each gets at least 64 units, else 6
+// with 33 KB rings.  Units are dealt round-robin, so the CTAs move through them in
+// order together.  Every
 // mbarrier wait has an iteration limit; past it the CTA records the failure in `err`,
 // stops issuing, waits (again with a limit) for the loads it has in flight and for its
 // stores, and returns.
@@ -39,9 +42,10 @@ namespace {
 
 constexpr int kTmaThreads = 32;                    // one warp; lane 0 drives the pipeline
 constexpr int kTmaMaxStages = 32;
-constexpr uint32_t kTmaSmemBudget = 200u * 1024u;  // dynamic shared memory of a CTA
+constexpr uint32_t kTmaSmemPerSm = 198u * 1024u;  // dynamic shared memory of the CTAs of one SM
 constexpr uint32_t kTmaMaxBox = 256;               // tensor-map box extent limit
 constexpr uint32_t kWaitRounds = 1u << 22;         // try_wait rounds before a load counts as lost
+constexpr int kUnitsPerCta = 64;                   // fewer units per CTA at 3 CTAs/SM: use 6 CTAs/SM
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p)
 {
@@ -97,10 +101,11 @@ __device__ __forceinline__ void bulk_store(void *gdst, uint32_t src, uint32_t by
 
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
-// All but the most recent group of bulk stores have finished reading shared memory.
-__device__ __forceinline__ void bulk_wait_read_all_but_one()
+// All but the PEND most recent groups of bulk stores have finished reading shared memory.
+template <int PEND>
+__device__ __forceinline__ void bulk_wait_read_older()
 {
-    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(PEND) : "memory");
 }
 
 // Every bulk store of this thread is complete.
@@ -139,7 +144,8 @@ __device__ __forceinline__ unit_id unit_of(const tdp_geom &g, int64_t u)
     return id;
 }
 
-__global__ void __launch_bounds__(kTmaThreads, 1)
+template <int PEND>
+__global__ void __launch_bounds__(kTmaThreads)
 tdp_split_tma_kernel(const __grid_constant__ CUtensorMap map, const __grid_constant__ tdp_geom g, int64_t n_units,
                      int32_t stages, uint32_t stage_stride, uint32_t box_bytes, char *__restrict__ Y,
                      int32_t *__restrict__ err)
@@ -196,9 +202,9 @@ tdp_split_tma_kernel(const __grid_constant__ CUtensorMap map, const __grid_const
             }
         }
         bulk_commit();
-        // refill the stage of unit i - 1, whose stores were committed one unit ago
-        if (i >= 1 && issued < n_mine) {
-            bulk_wait_read_all_but_one();
+        // refill the stage of unit i - PEND once its stores have read it
+        if (i >= PEND && issued < n_mine) {
+            bulk_wait_read_older<PEND>();
             issue_load(issued);
             ++issued;
         }
@@ -233,8 +239,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_tiled()
     return fn;
 }
 
-// CTAs resident per device at the given dynamic shared memory: one per SM.
-int32_t tma_grid(size_t smem)
+// Multiprocessors of the current device (0 on error).
+int32_t device_sms()
 {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -242,12 +248,20 @@ int32_t tma_grid(size_t smem)
         cudaGetLastError();
         return 0;
     }
-    if (cudaFuncSetAttribute(tdp_split_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess) {
-        cudaGetLastError();
-        return 0;
-    }
     return sms;
+}
+
+template <int PEND>
+cudaError_t launch_tma(unsigned grid, size_t smem, cudaStream_t s, const CUtensorMap &map, const tdp_geom &g,
+                       int64_t n_units, int32_t stages, uint32_t stage_stride, uint32_t box_bytes, void *Y,
+                       int32_t *err)
+{
+    cudaError_t ce = cudaFuncSetAttribute(tdp_split_tma_kernel<PEND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)smem);
+    if (ce != cudaSuccess) return ce;
+    // a plain launch: the copy starts once all earlier work in the stream has completed
+    return tdp_launch_smem(false, tdp_split_tma_kernel<PEND>, grid, kTmaThreads, smem, s, map, g, n_units, stages,
+                           stage_stride, box_bytes, static_cast<char *>(Y), err);
 }
 
 }  // namespace
@@ -265,10 +279,10 @@ extern "C" tdp_status tdp_split_tma(tdp_plan_t plan, const void *X, const int32_
     for (int32_t i = 0; i < g.d[2].n; ++i) box_w = g.d[2].hi[i] - g.d[2].lo[i] > box_w ? g.d[2].hi[i] - g.d[2].lo[i] : box_w;
     const uint32_t box_bytes = (uint32_t)g.C * (uint32_t)box_w * (uint32_t)g.esize;
     const uint32_t stage_stride = (box_bytes + 127u) & ~127u;      // stages start 128-byte aligned
-    if ((uint32_t)g.C > kTmaMaxBox || (uint32_t)box_w > kTmaMaxBox || 2 * (stage_stride + 8) > kTmaSmemBudget)
+    if ((uint32_t)g.C > kTmaMaxBox || (uint32_t)box_w > kTmaMaxBox || 2 * (stage_stride + 8) > kTmaSmemPerSm / 3)
         return tdp_fail(TDP_ERR_TOO_LARGE,
                         "tdp_split_tma needs C <= 256, W-tiles at most 256 cells and two boxes of the widest "
-                        "W-tile within 200 KB (tdp_split takes every shape)");
+                        "W-tile within 66 KB (tdp_split takes every shape)");
     PFN_cuTensorMapEncodeTiled_v12000 encode = encode_tiled();
     if (!encode) return tdp_fail(TDP_ERR_CUDA, "cuTensorMapEncodeTiled not available from the driver");
 
@@ -284,18 +298,28 @@ extern "C" tdp_status tdp_split_tma(tdp_plan_t plan, const void *X, const int32_
                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (cr != CUDA_SUCCESS) return tdp_fail(TDP_ERR_CUDA, "cuTensorMapEncodeTiled rejected the latent's tensor map");
 
-    int32_t stages = (int32_t)(kTmaSmemBudget / (stage_stride + 8));
+    // CTAs per SM: 3 with deeper rings when every CTA has many units, else 6 (the ramp of
+    // each CTA's ring then weighs more than its depth); at least two stages per CTA
+    const int32_t sms = device_sms();
+    if (sms <= 0) return tdp_fail(TDP_ERR_CUDA, "could not read the multiprocessor count");
+    const int64_t n_units = (int64_t)g.B * g.F * g.H * g.d[2].n;
+    int32_t per_sm = n_units >= (int64_t)3 * sms * kUnitsPerCta ? 3 : 6;
+    if (2 * (stage_stride + 8) > kTmaSmemPerSm / per_sm) per_sm = 3;
+    int32_t stages = (int32_t)(kTmaSmemPerSm / per_sm / (stage_stride + 8));
     stages = stages > kTmaMaxStages ? kTmaMaxStages : stages;
     const size_t smem = (size_t)stages * (stage_stride + 8);
-    const int32_t ctas = tma_grid(smem);
-    if (ctas <= 0) return tdp_fail(TDP_ERR_CUDA, "could not size the bulk-tensor split's grid");
-    const int64_t n_units = (int64_t)g.B * g.F * g.H * g.d[2].n;
+    const int64_t ctas = (int64_t)sms * per_sm;
     const unsigned grid = (unsigned)(n_units < ctas ? n_units : ctas);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // plain launch: the copy starts once all earlier work in the stream has completed
-    cudaError_t ce = tdp_launch_smem(false, tdp_split_tma_kernel, grid, kTmaThreads, smem, s, map, g, n_units,
-                                     stages, stage_stride, box_bytes, static_cast<char *>(Y), err);
-    if (ce == cudaSuccess && P) ce = tdp_launch_split_positions(g, P, normalize, Q, mn, s);
+    // groups of bulk stores in flight: 4, 2 or 1, leaving at least one stage to load into
+    cudaError_t ce;
+    if (stages > 4)
+        ce = launch_tma<4>(grid, smem, s, map, g, n_units, stages, stage_stride, box_bytes, Y, err);
+    else if (stages > 2)
+        ce = launch_tma<2>(grid, smem, s, map, g, n_units, stages, stage_stride, box_bytes, Y, err);
+    else
+        ce = launch_tma<1>(grid, smem, s, map, g, n_units, stages, stage_stride, box_bytes, Y, err);
+    if (ce == cudaSuccess && P) ce = tdp_launch_split_positions(g, P, normalize, Q, mn, s, true);
     if (ce == cudaSuccess) ce = cudaGetLastError();
     if (ce != cudaSuccess) return tdp_fail(TDP_ERR_CUDA, cudaGetErrorString(ce));
     return tdp_ok();

@@ -180,7 +180,7 @@ tdp_status tdp_split(tdp_plan_t plan, const void *X, const int32_t *P, const int
  *         within the kernel's wait limit (Y is then incomplete); never cleared by the
  *         library, so the caller zeroes it.
  * Shapes: C <= 256 elements and W-tiles at most 256 cells wide (tensor-map box
- * limits), two boxes of the widest W-tile within 200 KB of shared memory; other
+ * limits), two boxes of the widest W-tile within 66 KB of shared memory; other
  * shapes return TDP_ERR_TOO_LARGE (tdp_split takes every shape).  The first kernel
  * is an ordinary launch: it starts after all earlier work in the stream.
  */
@@ -307,6 +307,38 @@ tdp_status tdp_tile_mean(tdp_plan_t plan, int64_t L, const void *A, void *out, t
  *   stream CUDA stream.
  */
 tdp_status tdp_blend(tdp_plan_t plan, const void *Yout, void *Z, tdp_stream_t stream);
+
+/*
+ * tdp_blend_partial -- one rank's share of the blend when tiles are spread over ranks
+ * round-robin.
+ * ("What it is": tiles are assigned to ranks round-robin, tile t to rank t % world, and
+ *  a single all_reduce sums the ranks' blended tiles into the final result.)
+ *
+ * Zp[b,f,h,w,:] = sum over the tiles t covering the cell with t % world == rank, in
+ * ascending t, of mask * Yout (the masks of tdp_blend), in fp32; +0 where the rank owns
+ * no covering tile.  Summing the world ranks' Zp (the collective) and storing the sum
+ * with tdp_blend_store gives the blended latent; with world == 1 this is bit for bit
+ * tdp_blend.
+ *
+ *   rank, world  0 <= rank < world.
+ *   Yout         device tile-major tile outputs in tdp_split's layout (plan dtype); only the
+ *                rank's tiles are read, so the other tiles' entries need not be filled.
+ *   Zp           device [B,F,H,W,C] fp32, written (every element).  Must not overlap Yout.
+ *   stream       CUDA stream.
+ */
+tdp_status tdp_blend_partial(tdp_plan_t plan, int32_t rank, int32_t world, const void *Yout, float *Zp,
+                             tdp_stream_t stream);
+
+/*
+ * tdp_blend_store -- store a summed fp32 latent (or a slab of one) in the plan's dtype.
+ * ("What it is": the blended tiles, summed across ranks, are the final result.)
+ *
+ * Z[i] = Zsum[i] for i < n, rounded to nearest even for bf16 (a copy for fp32).
+ *   n      elements; a multiple of 16 bytes of the plan's dtype (8 bf16 or 4 fp32), so
+ *          any run of whole latent rows qualifies.
+ *   Zsum   device fp32 [n], read.   Z  device [n] (plan dtype), written.  16-byte aligned.
+ */
+tdp_status tdp_blend_store(tdp_plan_t plan, int64_t n, const float *Zsum, void *Z, tdp_stream_t stream);
 
 /*
  * Plan helpers (host only, no CUDA call).
