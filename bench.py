@@ -896,7 +896,17 @@ def main():
             os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK="0", WORLD_SIZE="1")
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
-    line = run_ours(args, rank, world, local_rank)
+    # stdout carries the one JSON line: whatever the libraries print while the arm runs
+    # (NCCL's version banner, for one) goes to stderr
+    sys.stdout.flush()
+    saved = os.dup(1)
+    os.dup2(2, 1)
+    try:
+        line = run_ours(args, rank, world, local_rank)
+    finally:
+        sys.stdout.flush()
+        os.dup2(saved, 1)
+        os.close(saved)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if distributed:

@@ -8,7 +8,12 @@
 // 2 x 2 x 2 tiles); its positions likewise, shifted by the tiles' mn when
 // normalising.  The scatter form reads the latent once instead of once per
 // covering tile, so the split moves B*T*C + B*sum(T_t)*C elements, its
-// algorithmic minimum.
+// algorithmic minimum.  The same split through the Tensor Memory Accelerator
+// (bulk-tensor loads of tile-row segments into shared memory, bulk stores to the
+// tiles) is tdp_split_tma in tdp_split_tma.cu: bit-identical, and on the large
+// workload (64x128x192x128 bf16, 2x8x8 tiles) 0.32 ms against this kernel's 0.29 ms,
+// its latent copy alone 0.260 ms against 0.267 ms.  These register-staged stores stay
+// the default.
 //
 // tdp_split_filter runs the whole pre-model stage in three launches:
 //   1. tdp_bounds_init_kernel   (plain launch)
