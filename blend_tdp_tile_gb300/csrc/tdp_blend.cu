@@ -118,7 +118,7 @@ tdp_blend_kernel(const __grid_constant__ tdp_geom g, int32_t cv_shift, const uin
     const int32_t nc = rc.nc;
     float rFH[TDP_MAX_COMBOS];
 #pragma unroll
-    for (int c = 0; c < TDP_MAX_COMBOS; ++c) rFH[c] = c < nc ? rc.rFH[c] : 0.0f;
+    for (int c = 0; c < TDP_MAX_COMBOS; ++c) rFH[c] = c < nc ? rc.rFH(c) : 0.0f;
 
     tdp_pdl_wait();                                   // Yout written by the work before
 
@@ -262,7 +262,7 @@ tdp_blend_partial_kernel(const __grid_constant__ tdp_geom g, int32_t rank, int32
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
                 const int32_t iW = k ? cW.i1 : cW.i0;
-                const int32_t t = c < rc.nc && iW >= 0 ? (rc.iF[c] * nH + rc.iH[c]) * nW + iW : -1;
+                const int32_t t = c < rc.nc && iW >= 0 ? (rc.iF(c) * nH + rc.iH(c)) * nW + iW : -1;
                 own[c][k] = t >= 0 && t % world == rank;
                 if (own[c][k]) y[c][k] = __ldcs(Yout + (s_tok[c * nW + iW] + w) * CV + cv);
             }
@@ -275,7 +275,7 @@ tdp_blend_partial_kernel(const __grid_constant__ tdp_geom g, int32_t rank, int32
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
                 if (!own[c][k]) continue;
-                const float m = rc.rFH[c] * (k ? r1 : r0);
+                const float m = rc.rFH(c) * (k ? r1 : r0);
                 if (first) VM::mul(acc, m, y[c][k]);           // the first term keeps the sign of zero
                 else VM::fma(acc, m, y[c][k]);
                 first = false;

@@ -74,8 +74,17 @@ __device__ __forceinline__ float tdp_weight(int32_t num, int32_t o)
 
 struct tdp_row_combos {
     int32_t nc;                           // combos (1, 2 or 4)
-    int32_t iF[TDP_MAX_COMBOS], iH[TDP_MAX_COMBOS];
-    float rFH[TDP_MAX_COMBOS];            // r_F * r_H of the combo
+    int32_t nH;                           // H-tiles per F-tile in the row (1 or 2)
+    int32_t iF0, iF1, iH0, iH1;           // covering F- and H-tiles (second = -1 when none)
+    float rF0, rF1, rH0, rH1;             // their ramp weights
+    // Combo c in ascending (iF, iH): F-tile c / nH, H-tile c % nH.  Scalars and selects
+    // rather than arrays, so that a combo index known only at run time needs no local memory.
+    __device__ __forceinline__ int32_t fsel(int32_t c) const { return nH == 2 ? c >> 1 : c; }
+    __device__ __forceinline__ int32_t hsel(int32_t c) const { return nH == 2 ? c & 1 : 0; }
+    __device__ __forceinline__ int32_t iF(int32_t c) const { return fsel(c) ? iF1 : iF0; }
+    __device__ __forceinline__ int32_t iH(int32_t c) const { return hsel(c) ? iH1 : iH0; }
+    // r_F * r_H of combo c
+    __device__ __forceinline__ float rFH(int32_t c) const { return (fsel(c) ? rF1 : rF0) * (hsel(c) ? rH1 : rH0); }
 };
 
 __device__ __forceinline__ tdp_row_combos tdp_make_combos(const tdp_geom &g, int32_t f, int32_t h)
@@ -83,17 +92,17 @@ __device__ __forceinline__ tdp_row_combos tdp_make_combos(const tdp_geom &g, int
     const tdp_cover cF = tdp_cover_1d(g.d[0], f);
     const tdp_cover cH = tdp_cover_1d(g.d[1], h);
     tdp_row_combos rc;
-    const int32_t nF = cF.i1 >= 0 ? 2 : 1, nH = cH.i1 >= 0 ? 2 : 1;
-    rc.nc = nF * nH;
-    int32_t c = 0;
-    for (int32_t a = 0; a < nF; ++a)
-        for (int32_t e = 0; e < nH; ++e, ++c) {
-            rc.iF[c] = a ? cF.i1 : cF.i0;
-            rc.iH[c] = e ? cH.i1 : cH.i0;
-            const float rF = tdp_weight(a ? cF.num1 : cF.num0, g.d[0].o);
-            const float rH = tdp_weight(e ? cH.num1 : cH.num0, g.d[1].o);
-            rc.rFH[c] = rF * rH;
-        }
+    const int32_t nF = cF.i1 >= 0 ? 2 : 1;
+    rc.nH = cH.i1 >= 0 ? 2 : 1;
+    rc.nc = nF * rc.nH;
+    rc.iF0 = cF.i0;
+    rc.iF1 = cF.i1;
+    rc.iH0 = cH.i0;
+    rc.iH1 = cH.i1;
+    rc.rF0 = tdp_weight(cF.num0, g.d[0].o);
+    rc.rF1 = tdp_weight(cF.num1, g.d[0].o);
+    rc.rH0 = tdp_weight(cH.num0, g.d[1].o);
+    rc.rH1 = tdp_weight(cH.num1, g.d[1].o);
     return rc;
 }
 
@@ -116,7 +125,7 @@ __device__ __forceinline__ void tdp_fill_row_table(const tdp_geom &g, const tdp_
     const int32_t nW = g.d[2].n;
     for (int32_t e = threadIdx.x; e < rc.nc * nW; e += blockDim.x) {
         const int32_t c = e / nW, iW = e % nW;
-        const int32_t iF = rc.iF[c], iH = rc.iH[c];
+        const int32_t iF = rc.iF(c), iH = rc.iH(c);
         const int64_t SH = g.d[1].hi[iH] - g.d[1].lo[iH];
         const int64_t SW = g.d[2].hi[iW] - g.d[2].lo[iW];
         const int64_t SF = g.d[0].hi[iF] - g.d[0].lo[iF];
