@@ -96,7 +96,7 @@ tdp_blend_kernel(const __grid_constant__ tdp_geom g, int32_t cv_shift, const uin
 {
     using VM = vec_math<BF16>;
     __shared__ int64_t s_tok[TDP_MAX_COMBOS * TDP_MAX_TILES_PER_DIM];
-    __shared__ tdp_wcell s_w[kWTab];
+    extern __shared__ tdp_wcell s_w[];                // min(W, kWTab) cells (dynamic)
     __shared__ int32_t s_loW[TDP_MAX_TILES_PER_DIM], s_hiW[TDP_MAX_TILES_PER_DIM];
     tdp_pdl_trigger();
     for (int32_t i = threadIdx.x; i < g.d[2].n; i += blockDim.x) {
@@ -372,8 +372,12 @@ extern "C" tdp_status tdp_blend(tdp_plan_t plan, const void *Yout, void *Z, tdp_
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const uint4 *y = reinterpret_cast<const uint4 *>(Yout);
     uint4 *z = reinterpret_cast<uint4 *>(Z);
-    cudaError_t err = g.dtype == TDP_BF16 ? tdp_launch(true, tdp_blend_kernel<1>, rows, kBlendThreads, s, g, cv_shift, y, z)
-                                          : tdp_launch(true, tdp_blend_kernel<0>, rows, kBlendThreads, s, g, cv_shift, y, z);
+    // the W-cell table is sized to the row (up to kWTab cells), so that short rows leave
+    // room for more blocks per SM
+    const size_t wsmem = (size_t)(g.W < kWTab ? g.W : kWTab) * sizeof(tdp_wcell);
+    cudaError_t err =
+        g.dtype == TDP_BF16 ? tdp_launch_smem(true, tdp_blend_kernel<1>, rows, kBlendThreads, wsmem, s, g, cv_shift, y, z)
+                            : tdp_launch_smem(true, tdp_blend_kernel<0>, rows, kBlendThreads, wsmem, s, g, cv_shift, y, z);
     if (err == cudaSuccess) err = cudaGetLastError();
     if (err != cudaSuccess) return tdp_fail(TDP_ERR_CUDA, cudaGetErrorString(err));
     return tdp_ok();

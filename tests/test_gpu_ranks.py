@@ -100,3 +100,40 @@ def test_store_of_a_row_slab_and_refusals(tdp):
     for rank, world in ((0, 0), (2, 2), (-1, 3)):
         with pytest.raises(tdp.TdpError, match="TDP_ERR_INVALID_ARG"):
             tdp.tdp_blend_partial(plan, rank, world, Yd, Zp)
+
+
+@pytest.mark.parametrize("mode", ["reduce_scatter", "all_reduce"])
+def test_blend_across_ranks_through_nccl_one_rank(tdp, mode):
+    """blend_tdp_tile_gb300.ranks.blend_across_ranks end to end on the GPU: the partial blend,
+    an NCCL collective over a one-rank group and the store.  With one rank every step is
+    exact, so the result equals tdp_blend bit for bit."""
+    import socket
+
+    import torch
+    import torch.distributed as dist
+
+    from blend_tdp_tile_gb300 import ranks
+    wl = wk.by_name("temporal")
+    plan, _, Yout = _case(tdp, wl)
+    Yd = to_dev(Yout)
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    group = dist.new_group(backend="nccl") if dist.is_initialized() else None
+    own_init = group is None
+    if own_init:
+        dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0, world_size=1,
+                                device_id=torch.device("cuda", torch.cuda.current_device()))
+    try:
+        Z = torch.empty((wl.B, wl.F, wl.H, wl.W, wl.C), dtype=torch.bfloat16, device="cuda")
+        s = torch.cuda.Stream()
+        used = ranks.blend_across_ranks(plan, Yd, Z, group=group, mode=mode, stream=s)
+        s.synchronize()
+        assert used == mode
+        Zref = torch.empty_like(Z)
+        tdp.tdp_blend(plan, Yd, Zref)
+        torch.cuda.synchronize()
+        assert torch.equal(Z.view(torch.int16), Zref.view(torch.int16))
+    finally:
+        if own_init:
+            dist.destroy_process_group()
