@@ -47,7 +47,7 @@ AUDIO_TOKENS = 2048          # synthetic per-tile audio latent for the tile-mean
 LAUNCHES_PER_STEP = {
     "fused": 4,       # bounds init, bounds, split + filter, blend
     "separate": 6,    # bounds init, bounds, split, keep, compact, blend
-    "tma": 7,         # bounds init, bounds, bulk-tensor split, split positions, keep, compact, blend
+    "tma": 6,         # bounds init, bounds, bulk-tensor split (latent and positions), keep, compact, blend
 }
 # --parallel round_robin replaces the blend by tdp_blend_partial + tdp_blend_store (one more)
 # ncu DRAM-traffic summaries, one per workload: profiles/dram_traffic_<workload>.txt
@@ -198,7 +198,6 @@ KERNEL_SOURCES = {
     "tdp_split_kernel": ["tdp_split.cu", "tdp_filter.cuh"] + _COMMON,
     "tdp_split_filter_kernel": ["tdp_split.cu", "tdp_filter.cuh"] + _COMMON,
     "tdp_split_tma_kernel": ["tdp_split_tma.cu"] + _COMMON,
-    "tdp_split_pos_kernel": ["tdp_split.cu", "tdp_filter.cuh"] + _COMMON,
     "tdp_bounds_init_kernel": ["tdp_bounds.cu"] + _COMMON,
     "tdp_bounds_kernel": ["tdp_bounds.cu"] + _COMMON,
 }
@@ -206,7 +205,7 @@ KERNEL_SOURCES = {
 CALL_KERNELS = {
     "tdp_split_filter": ["tdp_bounds_init_kernel", "tdp_bounds_kernel", "tdp_split_filter_kernel"],
     "tdp_split": ["tdp_split_kernel"],
-    "tdp_split_tma": ["tdp_split_tma_kernel", "tdp_split_pos_kernel"],
+    "tdp_split_tma": ["tdp_split_tma_kernel"],
     "tdp_blend": ["tdp_blend_kernel"],
 }
 

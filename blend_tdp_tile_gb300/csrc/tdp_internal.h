@@ -53,12 +53,6 @@ static inline cudaError_t tdp_launch(bool pdl, void (*kernel)(KArgs...), unsigne
 // on stream s: mn / mx of every (tile, batch item, dim).  Arguments checked by the caller.
 cudaError_t tdp_launch_bounds(const tdp_geom &g, const int32_t *P, int32_t *mn, int32_t *mx, cudaStream_t s);
 
-// tdp_split_pos_kernel on stream s: the tile positions alone, minus mn when normalising.
-// As a dependent launch (pdl) it must run right behind a plain launch that writes none of
-// P, mn, Q; otherwise it is a plain launch.
-cudaError_t tdp_launch_split_positions(const tdp_geom &g, const int32_t *P, int32_t normalize, int32_t *Q,
-                                       const int32_t *mn, cudaStream_t s, bool pdl);
-
 // Shared argument checks of the split entry points (host only).
 tdp_status tdp_check_split_args(const tdp_geom &g, const void *X, const int32_t *P, const int32_t *mn,
                                 int32_t normalize, const void *Y, const int32_t *Q);

@@ -149,22 +149,6 @@ tdp_split_kernel(const __grid_constant__ tdp_geom g, const uint4 *__restrict__ X
     if (P) split_positions(g, r, P, normalize, Q, mn, sm);
 }
 
-// Block = one latent row (b, f, h): positions only.  Launched by tdp_split_tma as a
-// dependent behind the bulk-tensor latent copy, which is a plain launch (it began after
-// all earlier work in the stream completed) and writes neither P, mn nor Q: the
-// positions therefore run beside that copy, and the wait at the end makes this kernel
-// complete only after the copy has, so that later work sees the whole split.
-__global__ void __launch_bounds__(kSplitThreads)
-tdp_split_pos_kernel(const __grid_constant__ tdp_geom g, const int2 *__restrict__ P, int32_t normalize,
-                     int2 *__restrict__ Q, const int32_t *__restrict__ mn)
-{
-    __shared__ split_smem sm;
-    tdp_pdl_trigger();
-    const split_row_id r = split_table(g, blockIdx.x, true, sm);
-    split_positions(g, r, P, normalize, Q, mn, sm);
-    tdp_pdl_wait();
-}
-
 // Blocks [0, fpos): split rows 0..fpos-1; [fpos, fpos + nfilt): filter blocks
 // (tb = t*B + b); [fpos + nfilt, fpos + nfilt + ncount): count blocks; the rest:
 // split rows fpos.. .  Split rows copy their latent before waiting on the bounds
@@ -223,14 +207,6 @@ int32_t resident_split_blocks()
 }
 
 }  // namespace
-
-cudaError_t tdp_launch_split_positions(const tdp_geom &g, const int32_t *P, int32_t normalize, int32_t *Q,
-                                       const int32_t *mn, cudaStream_t s, bool pdl)
-{
-    const int64_t rows = (int64_t)g.B * g.F * g.H;
-    return tdp_launch(pdl, tdp_split_pos_kernel, (unsigned)rows, kSplitThreads, s, g,
-                      reinterpret_cast<const int2 *>(P), normalize, reinterpret_cast<int2 *>(Q), mn);
-}
 
 tdp_status tdp_check_split_args(const tdp_geom &g, const void *X, const int32_t *P, const int32_t *mn,
                                 int32_t normalize, const void *Y, const int32_t *Q)

@@ -1,7 +1,7 @@
 // tdp_split_tma.cu -- tile split with the latent moved by the Tensor Memory Accelerator
 // ("Tiled Data Parallelism (TDP)", section "What it is": the patchified latent is split
-// into overlapping tiles; "Position normalization" for the positions, which run in
-// tdp_split_pos_kernel beside the copy).
+// into overlapping tiles; "Position normalization" for the positions, which the same
+// CTAs split beside the copy).
 //
 // A unit of work is one tile-row segment: batch item b, frame f, row h and W-tile iW,
 // i.e. the cells [lo_W, hi_W) of latent row (b, f, h), SW = hi_W - lo_W cells of C
@@ -18,16 +18,17 @@
 // overlap cells two neighbouring segments share are read from HBM once and from L2
 // the second time.
 //
-// One thread per CTA drives a ring of S stages: the bulk stores of the last PEND units
-// stay in flight (PEND = 4, 2 or 1 by ring depth), the other S - PEND stages hold loads
-// running ahead, and a stage is reloaded once the stores issued from it have finished
-// reading it (cp.async.bulk.wait_group.read).  One CTA's ring moves about 30 GB/s, so
-// an SM holds several: 3 CTAs with 66 KB rings when each gets at least 64 units, else 6
-// with 33 KB rings.  Units are dealt round-robin, so the CTAs move through them in
-// order together.  Every
-// mbarrier wait has an iteration limit; past it the CTA records the failure in `err`,
-// stops issuing, waits (again with a limit) for the loads it has in flight and for its
-// stores, and returns.
+// Warp 0 of a CTA copies the latent; warps 1..3 split the positions of their share of
+// the latent rows, a warp per row at a time, so that the positions run beside the copy
+// in the same launch.  One thread drives the latent's ring of S stages: the bulk stores
+// of the last PEND units stay in flight (PEND = 4, 2 or 1 by ring depth), the other
+// S - PEND stages hold loads running ahead, and a stage is reloaded once the stores
+// issued from it have finished reading it (cp.async.bulk.wait_group.read).  One CTA's
+// ring moves about 30 GB/s, so an SM holds several: 3 CTAs with 66 KB of shared memory
+// when each gets at least 64 units, else 6 with 33 KB.  Units are dealt round-robin, so
+// the CTAs move through them in order together.  Every mbarrier wait has an iteration
+// limit; past it the CTA records the failure in `err`, stops issuing, waits (again with
+// a limit) for the loads it has in flight and for its stores, and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -40,7 +41,8 @@
 
 namespace {
 
-constexpr int kTmaThreads = 32;                    // one warp; lane 0 drives the pipeline
+constexpr int kPosWarpsPerCta = 3;                 // warps of a CTA that split the positions
+constexpr int kTmaThreads = 32 * (1 + kPosWarpsPerCta);   // warp 0, lane 0 drives the latent pipeline
 constexpr int kTmaMaxStages = 32;
 constexpr uint32_t kTmaSmemPerSm = 198u * 1024u;  // dynamic shared memory of the CTAs of one SM
 constexpr uint32_t kTmaMaxBox = 256;               // tensor-map box extent limit
@@ -144,14 +146,104 @@ __device__ __forceinline__ unit_id unit_of(const tdp_geom &g, int64_t u)
     return id;
 }
 
+// Positions of one latent row (b, f, h) by one warp.  The warp first lists, in its table
+// in shared memory, where the row starts in each tile holding it (per F/H combo and
+// W-tile: the position-buffer index of cell w = 0, the tile's token count and its (tile,
+// batch) row of mn); its lanes then stride over the row's 3*W [start, end) pairs,
+// kPosBatch loads in flight each, and store every pair, minus the tile's mn when
+// normalising, to each tile holding it (at most 2 x 2 x 2).
+constexpr int kPosBatch = 4;
+
+struct pos_entry {
+    int64_t qpos;          // index of (d = 0, cell w = 0) of the row in the tile's positions
+    int64_t Tt;            // tokens of the tile
+    int32_t tb, pad;       // t * B + b
+};
+
+__device__ __forceinline__ void split_pos_row(const tdp_geom &g, int64_t row, const int2 *__restrict__ P,
+                                              int32_t normalize, int2 *__restrict__ Q,
+                                              const int32_t *__restrict__ mn, pos_entry *tab, int32_t lane)
+{
+    const int32_t nW = g.d[2].n;
+    const int32_t h = (int32_t)(row % g.H), f = (int32_t)((row / g.H) % g.F);
+    const int32_t b = (int32_t)(row / ((int64_t)g.H * g.F));
+    const tdp_row_combos rc = tdp_make_combos(g, f, h);
+    __syncwarp();                                     // the previous row's table is no longer read
+    for (int32_t e = lane; e < rc.nc * nW; e += 32) {
+        const int32_t c = e / nW, iW = e - c * nW;
+        const int32_t iF = rc.iF(c), iH = rc.iH(c);
+        const int64_t SF = g.d[0].hi[iF] - g.d[0].lo[iF];
+        const int64_t SH = g.d[1].hi[iH] - g.d[1].lo[iH];
+        const int64_t SW = g.d[2].hi[iW] - g.d[2].lo[iW];
+        pos_entry pe;
+        pe.Tt = SF * SH * SW;
+        pe.qpos = (int64_t)g.B * tdp_tile_off(g, iF, iH, iW) * 3 + (int64_t)b * 3 * pe.Tt +
+                  ((int64_t)(f - g.d[0].lo[iF]) * SH + (h - g.d[1].lo[iH])) * SW - g.d[2].lo[iW];
+        pe.tb = ((iF * g.d[1].n + iH) * nW + iW) * g.B + b;
+        pe.pad = 0;
+        tab[e] = pe;
+    }
+    __syncwarp();
+    const int64_t T = (int64_t)g.F * g.H * g.W;
+    const int2 *src = P + (int64_t)b * 3 * T + ((int64_t)f * g.H + h) * g.W;
+    const int32_t n = 3 * g.W;
+    for (int32_t q0 = lane; q0 < n; q0 += 32 * kPosBatch) {
+        int2 p[kPosBatch];
+#pragma unroll
+        for (int u = 0; u < kPosBatch; ++u) {
+            const int32_t q = q0 + 32 * u;
+            if (q < n) {
+                const int32_t d = q / g.W;
+                p[u] = __ldcs(src + (int64_t)d * T + (q - d * g.W));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kPosBatch; ++u) {
+            const int32_t q = q0 + 32 * u;
+            if (q >= n) break;
+            const int32_t d = q / g.W, w = q - d * g.W;
+            int32_t w0, w1;
+            cover2(g.d[2], w, w0, w1);
+            for (int32_t c = 0; c < rc.nc; ++c) {
+                for (int32_t k = 0; k < 2; ++k) {
+                    const int32_t iW = k ? w1 : w0;
+                    if (iW < 0) break;
+                    const pos_entry pe = tab[c * nW + iW];
+                    int2 o = p[u];
+                    if (normalize) {
+                        const int32_t m = __ldg(mn + (int64_t)pe.tb * 3 + d);
+                        o.x = (int32_t)((uint32_t)o.x - (uint32_t)m);
+                        o.y = (int32_t)((uint32_t)o.y - (uint32_t)m);
+                    }
+                    Q[pe.qpos + (int64_t)d * pe.Tt + w] = o;
+                }
+            }
+        }
+    }
+}
+
 template <int PEND>
 __global__ void __launch_bounds__(kTmaThreads)
 tdp_split_tma_kernel(const __grid_constant__ CUtensorMap map, const __grid_constant__ tdp_geom g, int64_t n_units,
                      int32_t stages, uint32_t stage_stride, uint32_t box_bytes, char *__restrict__ Y,
-                     int32_t *__restrict__ err)
+                     int32_t *__restrict__ err, const int2 *__restrict__ P, int32_t normalize,
+                     int2 *__restrict__ Q, const int32_t *__restrict__ mn)
 {
     extern __shared__ __align__(128) unsigned char dsm[];
-    tdp_pdl_trigger();                     // the positions kernel may start beside this one
+    tdp_pdl_trigger();
+    const int32_t warp = threadIdx.x >> 5;
+    if (warp > 0) {
+        // positions: warp w of CTA c takes rows (c * kPosWarpsPerCta + w - 1) + k * (grid x kPosWarpsPerCta)
+        if (P) {
+            pos_entry *tab = reinterpret_cast<pos_entry *>(dsm + (size_t)stages * (stage_stride + 8)) +
+                             (warp - 1) * TDP_MAX_COMBOS * g.d[2].n;
+            const int64_t rows = (int64_t)g.B * g.F * g.H;
+            for (int64_t r = (int64_t)blockIdx.x * kPosWarpsPerCta + warp - 1; r < rows;
+                 r += (int64_t)gridDim.x * kPosWarpsPerCta)
+                split_pos_row(g, r, P, normalize, Q, mn, tab, threadIdx.x & 31);
+        }
+        return;
+    }
     if (threadIdx.x != 0) return;
     const uint32_t stage0 = smem_addr(dsm);
     const uint32_t bar0 = stage0 + (uint32_t)stages * stage_stride;   // stages * 8 bytes of mbarriers
@@ -254,14 +346,15 @@ int32_t device_sms()
 template <int PEND>
 cudaError_t launch_tma(unsigned grid, size_t smem, cudaStream_t s, const CUtensorMap &map, const tdp_geom &g,
                        int64_t n_units, int32_t stages, uint32_t stage_stride, uint32_t box_bytes, void *Y,
-                       int32_t *err)
+                       int32_t *err, const int32_t *P, int32_t normalize, int32_t *Q, const int32_t *mn)
 {
     cudaError_t ce = cudaFuncSetAttribute(tdp_split_tma_kernel<PEND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           (int)smem);
     if (ce != cudaSuccess) return ce;
     // a plain launch: the copy starts once all earlier work in the stream has completed
     return tdp_launch_smem(false, tdp_split_tma_kernel<PEND>, grid, kTmaThreads, smem, s, map, g, n_units, stages,
-                           stage_stride, box_bytes, static_cast<char *>(Y), err);
+                           stage_stride, box_bytes, static_cast<char *>(Y), err, reinterpret_cast<const int2 *>(P),
+                           P ? normalize : 0, reinterpret_cast<int2 *>(Q), mn);
 }
 
 }  // namespace
@@ -279,10 +372,14 @@ extern "C" tdp_status tdp_split_tma(tdp_plan_t plan, const void *X, const int32_
     for (int32_t i = 0; i < g.d[2].n; ++i) box_w = g.d[2].hi[i] - g.d[2].lo[i] > box_w ? g.d[2].hi[i] - g.d[2].lo[i] : box_w;
     const uint32_t box_bytes = (uint32_t)g.C * (uint32_t)box_w * (uint32_t)g.esize;
     const uint32_t stage_stride = (box_bytes + 127u) & ~127u;      // stages start 128-byte aligned
-    if ((uint32_t)g.C > kTmaMaxBox || (uint32_t)box_w > kTmaMaxBox || 2 * (stage_stride + 8) > kTmaSmemPerSm / 3)
+    // shared memory of a CTA: its ring of stages (+ an mbarrier each), then the row tables of
+    // its position warps
+    const uint32_t tables = (uint32_t)(kPosWarpsPerCta * TDP_MAX_COMBOS * g.d[2].n * sizeof(pos_entry));
+    if ((uint32_t)g.C > kTmaMaxBox || (uint32_t)box_w > kTmaMaxBox ||
+        2 * (stage_stride + 8) + tables > kTmaSmemPerSm / 3)
         return tdp_fail(TDP_ERR_TOO_LARGE,
                         "tdp_split_tma needs C <= 256, W-tiles at most 256 cells and two boxes of the widest "
-                        "W-tile within 66 KB (tdp_split takes every shape)");
+                        "W-tile plus the position tables within 66 KB (tdp_split takes every shape)");
     PFN_cuTensorMapEncodeTiled_v12000 encode = encode_tiled();
     if (!encode) return tdp_fail(TDP_ERR_CUDA, "cuTensorMapEncodeTiled not available from the driver");
 
@@ -304,22 +401,21 @@ extern "C" tdp_status tdp_split_tma(tdp_plan_t plan, const void *X, const int32_
     if (sms <= 0) return tdp_fail(TDP_ERR_CUDA, "could not read the multiprocessor count");
     const int64_t n_units = (int64_t)g.B * g.F * g.H * g.d[2].n;
     int32_t per_sm = n_units >= (int64_t)3 * sms * kUnitsPerCta ? 3 : 6;
-    if (2 * (stage_stride + 8) > kTmaSmemPerSm / per_sm) per_sm = 3;
-    int32_t stages = (int32_t)(kTmaSmemPerSm / per_sm / (stage_stride + 8));
+    if (2 * (stage_stride + 8) + tables > kTmaSmemPerSm / per_sm) per_sm = 3;
+    int32_t stages = (int32_t)((kTmaSmemPerSm / per_sm - tables) / (stage_stride + 8));
     stages = stages > kTmaMaxStages ? kTmaMaxStages : stages;
-    const size_t smem = (size_t)stages * (stage_stride + 8);
+    const size_t smem = (size_t)stages * (stage_stride + 8) + tables;
     const int64_t ctas = (int64_t)sms * per_sm;
     const unsigned grid = (unsigned)(n_units < ctas ? n_units : ctas);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // groups of bulk stores in flight: 4, 2 or 1, leaving at least one stage to load into
     cudaError_t ce;
     if (stages > 4)
-        ce = launch_tma<4>(grid, smem, s, map, g, n_units, stages, stage_stride, box_bytes, Y, err);
+        ce = launch_tma<4>(grid, smem, s, map, g, n_units, stages, stage_stride, box_bytes, Y, err, P, normalize, Q, mn);
     else if (stages > 2)
-        ce = launch_tma<2>(grid, smem, s, map, g, n_units, stages, stage_stride, box_bytes, Y, err);
+        ce = launch_tma<2>(grid, smem, s, map, g, n_units, stages, stage_stride, box_bytes, Y, err, P, normalize, Q, mn);
     else
-        ce = launch_tma<1>(grid, smem, s, map, g, n_units, stages, stage_stride, box_bytes, Y, err);
-    if (ce == cudaSuccess && P) ce = tdp_launch_split_positions(g, P, normalize, Q, mn, s, true);
+        ce = launch_tma<1>(grid, smem, s, map, g, n_units, stages, stage_stride, box_bytes, Y, err, P, normalize, Q, mn);
     if (ce == cudaSuccess) ce = cudaGetLastError();
     if (ce != cudaSuccess) return tdp_fail(TDP_ERR_CUDA, cudaGetErrorString(ce));
     return tdp_ok();

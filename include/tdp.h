@@ -172,17 +172,17 @@ tdp_status tdp_split(tdp_plan_t plan, const void *X, const int32_t *P, const int
  *
  * Each tile-row segment (batch item, frame, row, W-tile) is one bulk-tensor load of a
  * box of a tensor map over X into a shared-memory stage, followed by one bulk store
- * to each tile that holds the row (the segment is contiguous in Y).  The positions
- * run beside the copy in a second kernel.
+ * to each tile that holds the row (the segment is contiguous in Y).  Other warps of the
+ * same CTAs split the positions beside the copy.  One ordinary launch.
  *
  *   X, P, mn, normalize, Y, Q, stream   as for tdp_split.
  *   err   device int32, or NULL: set to 1 if a bulk-tensor load did not complete
  *         within the kernel's wait limit (Y is then incomplete); never cleared by the
  *         library, so the caller zeroes it.
  * Shapes: C <= 256 elements and W-tiles at most 256 cells wide (tensor-map box
- * limits), two boxes of the widest W-tile within 66 KB of shared memory; other
- * shapes return TDP_ERR_TOO_LARGE (tdp_split takes every shape).  The first kernel
- * is an ordinary launch: it starts after all earlier work in the stream.
+ * limits), two boxes of the widest W-tile and the position tables within 66 KB of
+ * shared memory; other shapes return TDP_ERR_TOO_LARGE (tdp_split takes every shape).
+ * The kernel is an ordinary launch: it starts after all earlier work in the stream.
  */
 tdp_status tdp_split_tma(tdp_plan_t plan, const void *X, const int32_t *P, const int32_t *mn, int32_t normalize,
                          void *Y, int32_t *Q, int32_t *err, tdp_stream_t stream);
