@@ -348,9 +348,21 @@ cudaError_t launch_tma(unsigned grid, size_t smem, cudaStream_t s, const CUtenso
                        int64_t n_units, int32_t stages, uint32_t stage_stride, uint32_t box_bytes, void *Y,
                        int32_t *err, const int32_t *P, int32_t normalize, int32_t *Q, const int32_t *mn)
 {
-    cudaError_t ce = cudaFuncSetAttribute(tdp_split_tma_kernel<PEND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          (int)smem);
+    // raise the kernel's shared-memory limit once per device and size (not on every call, so
+    // that calls after the first on a device make no attribute change, e.g. during capture)
+    static std::atomic<int> raised[64];
+    int dev = 0;
+    cudaError_t ce = cudaGetDevice(&dev);
     if (ce != cudaSuccess) return ce;
+    if (dev >= 64 || raised[dev].load(std::memory_order_relaxed) < (int)smem) {
+        ce = cudaFuncSetAttribute(tdp_split_tma_kernel<PEND>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (ce != cudaSuccess) return ce;
+        if (dev < 64) {
+            int cur = raised[dev].load(std::memory_order_relaxed);
+            while (cur < (int)smem && !raised[dev].compare_exchange_weak(cur, (int)smem)) {
+            }
+        }
+    }
     // a plain launch: the copy starts once all earlier work in the stream has completed
     return tdp_launch_smem(false, tdp_split_tma_kernel<PEND>, grid, kTmaThreads, smem, s, map, g, n_units, stages,
                            stage_stride, box_bytes, static_cast<char *>(Y), err, reinterpret_cast<const int2 *>(P),

@@ -183,6 +183,8 @@ tdp_status tdp_split(tdp_plan_t plan, const void *X, const int32_t *P, const int
  * limits), two boxes of the widest W-tile and the position tables within 66 KB of
  * shared memory; other shapes return TDP_ERR_TOO_LARGE (tdp_split takes every shape).
  * The kernel is an ordinary launch: it starts after all earlier work in the stream.
+ * The first call on a device looks up the driver's tensor-map encoder and raises the
+ * kernel's shared-memory limit; make it before capturing a stream into a CUDA graph.
  */
 tdp_status tdp_split_tma(tdp_plan_t plan, const void *X, const int32_t *P, const int32_t *mn, int32_t normalize,
                          void *Y, int32_t *Q, int32_t *err, tdp_stream_t stream);

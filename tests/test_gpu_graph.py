@@ -1,5 +1,6 @@
-"""One TDP step (bounds, split, filter, blend; as separate calls or with tdp_split_filter;
-then the conditioning blend and the tile mean) captured in a CUDA graph and replayed gives
+"""One TDP step (bounds, split, filter, blend; as separate calls, with tdp_split_filter or with
+tdp_split_tma; then the conditioning blend, the tile mean, and one rank's partial blend and
+its store) captured in a CUDA graph and replayed gives
 the same bytes as the same calls launched directly: the library allocates nothing and
 never synchronises, so its calls can sit inside a captured per-step graph."""
 import numpy as np
@@ -11,8 +12,8 @@ from gpu_path import to_dev
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("fused", [False, True])
-def test_graph_replay_matches_direct_launches(fused):
+@pytest.mark.parametrize("path", ["separate", "fused", "tma"])
+def test_graph_replay_matches_direct_launches(path):
     import torch
 
     import __graft_entry__
@@ -35,18 +36,25 @@ def test_graph_replay_matches_direct_launches(fused):
         Z = torch.empty_like(Xd)
         Oc = torch.empty((wl.B, N, wl.C), dtype=torch.bfloat16, device="cuda")
         Om = torch.empty((wl.B, La), dtype=torch.bfloat16, device="cuda")
-        return [Y, Q, mn, mx, *f, Z, Oc, Om]
+        Zp = torch.empty(Xd.shape, dtype=torch.float32, device="cuda")
+        Zr = torch.empty_like(Xd)
+        return [Y, Q, mn, mx, *f, Z, Oc, Om, Zp, Zr]
 
     def step(b, s):
-        Y, Q, mn, mx, keep, idx, count, kcount, Kout, slot, Z, Oc, Om = b
-        if fused:
+        Y, Q, mn, mx, keep, idx, count, kcount, Kout, slot, Z, Oc, Om, Zp, Zr = b
+        if path == "fused":
             tdp.tdp_split_filter(plan, Xd, Pd, Kd, N, 1, Y, Q, mn, mx, keep, idx, count, kcount, Kout, slot,
                                  stream=s)
         else:
             tdp.tdp_pos_bounds(plan, Pd, mn, mx, stream=s)
-            tdp.tdp_split(plan, Xd, Pd, mn, 1, Y, Q, stream=s)
+            if path == "tma":
+                tdp.tdp_split_tma(plan, Xd, Pd, mn, 1, Y, Q, stream=s)
+            else:
+                tdp.tdp_split(plan, Xd, Pd, mn, 1, Y, Q, stream=s)
             tdp.tdp_norm_filter(plan, Kd, N, mn, mx, 1, keep, idx, count, kcount, Kout, slot, stream=s)
         tdp.tdp_blend(plan, Yout, Z, stream=s)
+        tdp.tdp_blend_partial(plan, 0, 1, Yout, Zp, stream=s)       # one rank's share, then its store
+        tdp.tdp_blend_store(plan, Zp, Zr, stream=s)
         tdp.tdp_cond_blend(plan, N, ncap, Ycond, slot, Oc, stream=s)
         tdp.tdp_tile_mean(plan, La, A, Om, stream=s)
 
@@ -67,7 +75,8 @@ def test_graph_replay_matches_direct_launches(fused):
     for _ in range(2):
         g.replay()
     torch.cuda.synchronize()
-    names = ["Y", "Q", "mn", "mx", "keep", "idx", "count", "kcount", "Kout", "slot", "Z", "cond", "mean"]
+    names = ["Y", "Q", "mn", "mx", "keep", "idx", "count", "kcount", "Kout", "slot", "Z", "cond", "mean",
+             "Zpartial", "Zstored"]
     for name, a, b in zip(names, direct, graphed):
         if name == "Kout":   # entries past count are unspecified: compare the kept ones
             c = direct[6].cpu().numpy()

@@ -328,3 +328,24 @@ def test_split_tma_without_positions_and_refusals(tdp):
     Yw, _, _, _ = tdp.alloc_split_outputs(pw, "cuda", positions=False)
     with pytest.raises(tdp.TdpError, match="TDP_ERR_TOO_LARGE"):
         tdp.tdp_split_tma(pw, Xw, None, None, 1, Yw, None)
+
+
+def test_split_tma_at_the_w_tile_limit(tdp):
+    """64 W-tiles (the most a dimension takes) of one or two cells and f32 storage: the
+    position warps' row tables are at their largest, the boxes at their smallest."""
+    import torch
+    wl = wk.by_name("tiny").replace(B=2, F=3, H=5, W=128, C=16, num_tiles=(1, 2, 64), overlap=(0, 1, 1), n_cond=8)
+    X, P, _ = wk.make_inputs(wl)
+    plan = _plan(tdp, wl)
+    p = oracle.problem_of(wl)
+    Yref, Qref = oracle.split(p, X, P)
+    mn, _ = oracle.bounds(p, Qref)
+    Y, Q, _, _ = tdp.alloc_split_outputs(plan, "cuda")
+    for t in (Y, Q):
+        fill_sentinel(t)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    tdp.tdp_split_tma(plan, to_dev(X), to_dev(P), to_dev(mn), 1, Y, Q, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert np.array_equal(to_host(Y).reshape(Yref.shape), Yref)
+    assert np.array_equal(to_host(Q), oracle.normalize(p, Qref, mn))
