@@ -16,6 +16,8 @@
 // F/H combos a thread takes four (one combo) or two (two combos) vectors per
 // pass, up to 8 loads in flight, with 80 registers and 24 warps per SM (six
 // 128-thread blocks, so that more rows are in flight at once).
+#include <atomic>
+
 #include "tdp.h"
 #include "tdp_device.cuh"
 #include "tdp_internal.h"
@@ -25,6 +27,7 @@ namespace {
 constexpr int kBlendThreads = 128;
 constexpr int kWTab = 1024;      // cells of the per-row W table built per pass
 constexpr int kBlendMinBlocks = 6;   // blocks per SM the register budget is sized for
+constexpr size_t kBlendStage = 2 * 8 * kBlendThreads * 16;   // two passes of eight 16-byte slots per thread
 
 // W-coverage of one cell: tiles iW0 (low 16 bits) and iW1 + 1 (high 16 bits,
 // 0 = none) and their ramp weights.
@@ -89,6 +92,14 @@ struct vec_math<1> {     // 8 x bf16
     }
 };
 
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
 template <int BF16>
 __global__ void __launch_bounds__(kBlendThreads, kBlendMinBlocks)
 tdp_blend_kernel(const __grid_constant__ tdp_geom g, int32_t cv_shift, const uint4 *__restrict__ Yout,
@@ -96,7 +107,12 @@ tdp_blend_kernel(const __grid_constant__ tdp_geom g, int32_t cv_shift, const uin
 {
     using VM = vec_math<BF16>;
     __shared__ int64_t s_tok[TDP_MAX_COMBOS * TDP_MAX_TILES_PER_DIM];
-    extern __shared__ tdp_wcell s_w[];                // min(W, kWTab) cells (dynamic)
+    extern __shared__ __align__(16) unsigned char dsm[];
+    // dynamic: the W-cell table (min(W, kWTab) cells), then the load slots of the passes
+    tdp_wcell *s_w = reinterpret_cast<tdp_wcell *>(dsm);
+    const int32_t wtab = g.W < kWTab ? g.W : kWTab;
+    unsigned char *dsm_stage = dsm + (size_t)wtab * sizeof(tdp_wcell);
+    const uint32_t stage = static_cast<uint32_t>(__cvta_generic_to_shared(dsm_stage));
     __shared__ int32_t s_loW[TDP_MAX_TILES_PER_DIM], s_hiW[TDP_MAX_TILES_PER_DIM];
     tdp_pdl_trigger();
     for (int32_t i = threadIdx.x; i < g.d[2].n; i += blockDim.x) {
@@ -138,75 +154,53 @@ tdp_blend_kernel(const __grid_constant__ tdp_geom g, int32_t cv_shift, const uin
         const uint4 *ybase = Yout + (int64_t)wbase * CV;
         uint4 *zbase = Z + ((int64_t)b * T + ((int64_t)f * g.H + h) * g.W + wbase) * CV;
         const int32_t nvec = wn * CV;
-        if (nc <= 2) {
-            // At most one F- or H-overlap on this row: four load slots of two W-tiles
-            // each.  One combo: slot s is vector s (4 vectors per pass); two combos:
-            // slot s is combo s & 1 of vector s >> 1 (2 vectors per pass).  Every load
-            // of the pass is in flight before any arithmetic; each sum is formed in the
-            // same order as in the general loop.
-            const int32_t vpp = nc == 1 ? 4 : 2;           // vectors per pass (block-uniform)
-            for (int32_t v0 = threadIdx.x; v0 < nvec; v0 += vpp * (int32_t)blockDim.x) {
-                int32_t vq[4], iw[4];
-                uint4 y[4][2];                             // [slot][W-tile]
+        // Eight load slots per pass, copied global -> shared memory with cp.async (no
+        // registers held while in flight), two passes' slots per thread: a thread issues
+        // pass p + 1's copies before it sums pass p.  Slot s of a pass is W-tile s & 1 of
+        // combo (s >> 1) & (nc - 1) of the pass's vector s >> (1 + log2 nc): 4, 2 or 1
+        // vectors per pass for 1, 2 or 4 combos.  Each sum is formed in ascending tile
+        // order, combo by combo, as in tdp_blend's definition.
+        const int32_t lq = 1 + (nc >> 1);                 // log2 of the slots per vector
+        const int32_t step = (8 >> lq) * (int32_t)blockDim.x;
+        auto issue = [&](int32_t v0, int32_t buf) {
 #pragma unroll
-                for (int sl = 0; sl < 4; ++sl) {
-                    const int32_t qv = nc == 1 ? sl : sl >> 1, c = nc == 1 ? 0 : sl & 1;
-                    const int32_t v = v0 + qv * (int32_t)blockDim.x;
-                    vq[sl] = v < nvec ? v : v0;            // past the end: repeat vector v0
-                    iw[sl] = s_w[cv_shift >= 0 ? (vq[sl] >> cv_shift) : vq[sl] / CV].iw;
-                    const int32_t i0 = iw[sl] & 0xffff, i1 = (iw[sl] >> 16) - 1;
-                    if (v < nvec) {
-                        y[sl][0] = __ldcs(ybase + s_tok[c * nW + i0] + vq[sl]);
-                        if (i1 >= 0) y[sl][1] = __ldcs(ybase + s_tok[c * nW + i1] + vq[sl]);
-                    }
-                }
-                if (nc == 1) {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        if (v0 + q * (int32_t)blockDim.x >= nvec) break;
-                        const tdp_wcell e = s_w[cv_shift >= 0 ? (vq[q] >> cv_shift) : vq[q] / CV];
-                        float acc[VM::kElems];
-                        VM::mul(acc, rFH[0] * e.r0, y[q][0]);
-                        if ((iw[q] >> 16) != 0) VM::fma(acc, rFH[0] * e.r1, y[q][1]);
-                        __stcs(zbase + vq[q], VM::pack(acc));
-                    }
-                } else {
-#pragma unroll
-                    for (int q = 0; q < 2; ++q) {
-                        if (v0 + q * (int32_t)blockDim.x >= nvec) break;
-                        const int32_t sl = 2 * q;
-                        const tdp_wcell e = s_w[cv_shift >= 0 ? (vq[sl] >> cv_shift) : vq[sl] / CV];
-                        const bool two = (iw[sl] >> 16) != 0;
-                        float acc[VM::kElems];
-                        VM::mul(acc, rFH[0] * e.r0, y[sl][0]);
-                        if (two) VM::fma(acc, rFH[0] * e.r1, y[sl][1]);
-                        VM::fma(acc, rFH[1] * e.r0, y[sl + 1][0]);
-                        if (two) VM::fma(acc, rFH[1] * e.r1, y[sl + 1][1]);
-                        __stcs(zbase + vq[sl], VM::pack(acc));
-                    }
+            for (int sl = 0; sl < 8; ++sl) {
+                const int32_t v = v0 + (sl >> lq) * (int32_t)blockDim.x;
+                if (v < nvec) {
+                    const int32_t iw = s_w[cv_shift >= 0 ? (v >> cv_shift) : v / CV].iw;
+                    const int32_t iWx = (sl & 1) ? (iw >> 16) - 1 : (iw & 0xffff);
+                    if (iWx >= 0)
+                        cp_async16(stage + ((buf * 8 + sl) * kBlendThreads + threadIdx.x) * 16u,
+                                   ybase + s_tok[((sl >> 1) & (nc - 1)) * nW + iWx] + v);
                 }
             }
-        } else {
-            for (int32_t v = threadIdx.x; v < nvec; v += blockDim.x) {
-                const tdp_wcell e = s_w[cv_shift >= 0 ? (v >> cv_shift) : v / CV];
-                const int32_t iW0 = e.iw & 0xffff, iW1 = (e.iw >> 16) - 1;
-                // every load first (at most 8 in flight), then the arithmetic
-                uint4 y0[TDP_MAX_COMBOS], y1[TDP_MAX_COMBOS];
+            cp_async_commit();
+        };
+        int32_t buf = 0;
+        if ((int32_t)threadIdx.x < nvec) issue(threadIdx.x, 0);
+        for (int32_t v0 = threadIdx.x; v0 < nvec; v0 += step, buf ^= 1) {
+            if (v0 + step < nvec) {
+                issue(v0 + step, buf ^ 1);
+                cp_async_wait<1>();
+            } else {
+                cp_async_wait<0>();
+            }
+            const uint4 *sb = reinterpret_cast<const uint4 *>(dsm_stage) + (buf * 8) * kBlendThreads + threadIdx.x;
 #pragma unroll
-                for (int c = 0; c < TDP_MAX_COMBOS; ++c) {
-                    if (c < nc) {
-                        y0[c] = __ldcs(ybase + s_tok[c * nW + iW0] + v);
-                        if (iW1 >= 0) y1[c] = __ldcs(ybase + s_tok[c * nW + iW1] + v);
-                    }
-                }
+            for (int q = 0; q < 4; ++q) {
+                const int32_t v = v0 + q * (int32_t)blockDim.x;
+                if (q >= (8 >> lq) || v >= nvec) break;
+                const tdp_wcell e = s_w[cv_shift >= 0 ? (v >> cv_shift) : v / CV];
+                const bool two = (e.iw >> 16) != 0;
+                const int32_t s0 = q << lq;
                 float acc[VM::kElems];
-                VM::mul(acc, rFH[0] * e.r0, y0[0]);          // the first term keeps the sign of zero
-                if (iW1 >= 0) VM::fma(acc, rFH[0] * e.r1, y1[0]);
+                VM::mul(acc, rFH[0] * e.r0, sb[s0 * kBlendThreads]);          // the first term keeps the sign of zero
+                if (two) VM::fma(acc, rFH[0] * e.r1, sb[(s0 + 1) * kBlendThreads]);
 #pragma unroll
                 for (int c = 1; c < TDP_MAX_COMBOS; ++c) {
                     if (c < nc) {
-                        VM::fma(acc, rFH[c] * e.r0, y0[c]);
-                        if (iW1 >= 0) VM::fma(acc, rFH[c] * e.r1, y1[c]);
+                        VM::fma(acc, rFH[c] * e.r0, sb[(s0 + 2 * c) * kBlendThreads]);
+                        if (two) VM::fma(acc, rFH[c] * e.r1, sb[(s0 + 2 * c + 1) * kBlendThreads]);
                     }
                 }
                 __stcs(zbase + v, VM::pack(acc));
@@ -311,6 +305,26 @@ tdp_blend_store_kernel(int64_t nvec, const float4 *__restrict__ Zsum, uint4 *__r
     }
 }
 
+// Raise `kernel`'s dynamic shared-memory limit to `bytes` once per device (calls after the
+// first with a given size make no attribute change).
+template <typename K>
+cudaError_t allow_blend_smem(K kernel, size_t bytes)
+{
+    static std::atomic<int> raised[2][64];
+    const int which = kernel == reinterpret_cast<K>(tdp_blend_kernel<1>) ? 1 : 0;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 64 && raised[which][dev].load(std::memory_order_relaxed) >= (int)bytes) return cudaSuccess;
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (err == cudaSuccess && dev < 64) {
+        int cur = raised[which][dev].load(std::memory_order_relaxed);
+        while (cur < (int)bytes && !raised[which][dev].compare_exchange_weak(cur, (int)bytes)) {
+        }
+    }
+    return err;
+}
+
 }  // namespace
 
 extern "C" tdp_status tdp_blend_partial(tdp_plan_t plan, int32_t rank, int32_t world, const void *Yout, float *Zp,
@@ -374,10 +388,12 @@ extern "C" tdp_status tdp_blend(tdp_plan_t plan, const void *Yout, void *Z, tdp_
     uint4 *z = reinterpret_cast<uint4 *>(Z);
     // the W-cell table is sized to the row (up to kWTab cells), so that short rows leave
     // room for more blocks per SM
-    const size_t wsmem = (size_t)(g.W < kWTab ? g.W : kWTab) * sizeof(tdp_wcell);
-    cudaError_t err =
-        g.dtype == TDP_BF16 ? tdp_launch_smem(true, tdp_blend_kernel<1>, rows, kBlendThreads, wsmem, s, g, cv_shift, y, z)
-                            : tdp_launch_smem(true, tdp_blend_kernel<0>, rows, kBlendThreads, wsmem, s, g, cv_shift, y, z);
+    const size_t wsmem = (size_t)(g.W < kWTab ? g.W : kWTab) * sizeof(tdp_wcell) + kBlendStage;
+    cudaError_t err = g.dtype == TDP_BF16 ? allow_blend_smem(tdp_blend_kernel<1>, wsmem) : allow_blend_smem(tdp_blend_kernel<0>, wsmem);
+    if (err == cudaSuccess)
+        err = g.dtype == TDP_BF16
+                  ? tdp_launch_smem(true, tdp_blend_kernel<1>, rows, kBlendThreads, wsmem, s, g, cv_shift, y, z)
+                  : tdp_launch_smem(true, tdp_blend_kernel<0>, rows, kBlendThreads, wsmem, s, g, cv_shift, y, z);
     if (err == cudaSuccess) err = cudaGetLastError();
     if (err != cudaSuccess) return tdp_fail(TDP_ERR_CUDA, cudaGetErrorString(err));
     return tdp_ok();
