@@ -902,16 +902,16 @@ def main():
     os.dup2(2, 1)
     try:
         line = run_ours(args, rank, world, local_rank)
+        if distributed:
+            import torch.distributed as dist
+            dist.barrier()
+            dist.destroy_process_group()
     finally:
         sys.stdout.flush()
         os.dup2(saved, 1)
         os.close(saved)
     if rank == 0:
         print(json.dumps(line), flush=True)
-    if distributed:
-        import torch.distributed as dist
-        dist.barrier()
-        dist.destroy_process_group()
 
 
 if __name__ == "__main__":
