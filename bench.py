@@ -647,6 +647,19 @@ def run_ours(args, rank, world, local_rank):
              (plan.n_tiles + 1) * wl.B * La * wl.esize)):
             extras[name] = call_entry(call_ms(torch, s, fn, reps, flush), nbytes, peak)
             extras[name]["timing"] = f"mean of {reps} launches, each after an L2 flush"
+        # the post-model stage in one call (blend + conditioning blend, one launch) against
+        # the same two calls one after the other
+        cond_bytes = extras["cond_blend"]["algorithmic_bytes"]
+        Zx = torch.empty_like(Z)
+        fused_ms = call_ms(torch, s, lambda: tdp.tdp_blend_cond(plan, Yout, Zx, N, ncap, Yc, slot2, Oc, stream=s),
+                           reps, flush)
+        pair_ms = call_ms(torch, s, lambda: (tdp.tdp_blend(plan, Yout, Zx, stream=s),
+                                             tdp.tdp_cond_blend(plan, N, ncap, Yc, slot2, Oc, stream=s)), reps, flush)
+        extras["blend_cond"] = call_entry(fused_ms, ab["blend"] + cond_bytes, peak)
+        extras["blend_cond"].update({"two_calls_ms": pair_ms,
+                                     "timing": f"mean of {reps} launches, each after an L2 flush",
+                                     "calls": "tdp_blend_cond (one launch) against tdp_blend + tdp_cond_blend"})
+        del Zx
         # what the same timing gives a kernel that does almost nothing: the part of each
         # figure above that is launch and ramp, not bytes
         tiny = torch.zeros(8, device=dev)

@@ -27,7 +27,7 @@ __all__ = [
     "TDP_OK", "TDP_F32", "TDP_BF16", "TDP_MAX_TILES_PER_DIM", "TdpError",
     "Plan", "tdp_plan_create", "tdp_plan_info", "tdp_plan_destroy",
     "tdp_pos_bounds", "tdp_split", "tdp_split_tma", "tdp_norm_filter", "tdp_split_filter", "tdp_blend", "tdp_cond_blend",
-    "tdp_tile_mean", "tdp_blend_partial", "tdp_blend_store",
+    "tdp_tile_mean", "tdp_blend_partial", "tdp_blend_store", "tdp_blend_cond",
     "tdp_balanced_tile_split", "tdp_tiles_for_size", "tdp_rank_tiles",
     "tdp_status_str", "tdp_last_error_detail",
     "alloc_split_outputs", "alloc_filter_outputs", "LIB_PATH",
@@ -83,6 +83,8 @@ def _load():
     lib.tdp_tile_mean.restype = ctypes.c_int
     lib.tdp_blend.argtypes = [vp, vp, vp, vp]
     lib.tdp_blend.restype = ctypes.c_int
+    lib.tdp_blend_cond.argtypes = [vp, vp, vp, i32, i32, vp, vp, vp, vp]
+    lib.tdp_blend_cond.restype = ctypes.c_int
     lib.tdp_blend_partial.argtypes = [vp, i32, i32, vp, vp, vp]
     lib.tdp_blend_partial.restype = ctypes.c_int
     lib.tdp_blend_store.argtypes = [vp, ctypes.c_int64, vp, vp, vp]
@@ -406,6 +408,21 @@ def tdp_blend(plan: Plan, Yout, Z, stream=None):
     c = _Call("tdp_blend")
     c.run(_lib.tdp_blend, plan.handle, c.ptr(Yout, "Yout", B * tot * C, lat, 16),
           c.ptr(Z, "Z", B * T * C, lat, 16), stream=stream)
+
+
+def tdp_blend_cond(plan: Plan, Yout, Z, N, ncap, Ycond, slot, out, stream=None):
+    """tdp_blend (Yout -> Z) and tdp_cond_blend (Ycond, slot -> out) in one call (one launch):
+    the same outputs, bit for bit."""
+    torch = _torch()
+    B, T, C, nt, tot = plan.B, plan.F * plan.H * plan.W, plan.C, plan.n_tiles, plan.total_tile_tokens
+    N, ncap = int(N), int(ncap)
+    lat = _latent_dtypes(plan)
+    c = _Call("tdp_blend_cond")
+    c.run(_lib.tdp_blend_cond, plan.handle, c.ptr(Yout, "Yout", B * tot * C, lat, 16),
+          c.ptr(Z, "Z", B * T * C, lat, 16), N, ncap,
+          c.ptr(Ycond, "Ycond", nt * B * ncap * C, lat, 16),
+          c.ptr(slot, "slot", nt * B * N, (torch.int32,), 4),
+          c.ptr(out, "out", B * N * C, lat, 16), stream=stream)
 
 
 def tdp_blend_partial(plan: Plan, rank, world, Yout, Zp, stream=None):

@@ -274,6 +274,24 @@ tdp_status tdp_cond_blend(tdp_plan_t plan, int32_t N, int32_t ncap, const void *
                           const int32_t *slot, void *out, tdp_stream_t stream);
 
 /*
+ * tdp_blend_cond -- the post-model stage in one call: tdp_blend and tdp_cond_blend with
+ * the same arguments and bit-identical results, in one launch instead of two.
+ * ("What it is": the blended tiles are summed into the final result; "Shared negative
+ *  (reference) positions": a conditioning token's outputs weigh 1/(tiles that kept it).)
+ *
+ *   Yout, Z                  as for tdp_blend.
+ *   N, ncap, Ycond, slot, out as for tdp_cond_blend (N = 0: only the blend).
+ *   stream                   CUDA stream.
+ * The token blocks, latency-bound, run beside the bandwidth-bound latent rows in the
+ * same grid.  With more than 256 tiles, or Ycond rows numbered past 2^32, it issues the
+ * two calls one after the other.  Buffers must not overlap one another.  The first call
+ * on a device raises the kernel's shared-memory limit; make it before capturing a stream
+ * into a CUDA graph.
+ */
+tdp_status tdp_blend_cond(tdp_plan_t plan, const void *Yout, void *Z, int32_t N, int32_t ncap, const void *Ycond,
+                          const int32_t *slot, void *out, tdp_stream_t stream);
+
+/*
  * tdp_tile_mean -- mean over tiles of a per-tile untiled output (the audio path).
  * ("What it is": audio is processed untiled on every tile's forward pass and
  *  averaged across tiles; the page warns that this average is context for the

@@ -9,7 +9,8 @@ guard band of GUARD bytes on each side:
   element-by-element comparison with the CPU oracle would fail.
 
 Each case runs every entry point: tdp_pos_bounds, tdp_split, tdp_split_tma,
-tdp_norm_filter, tdp_split_filter, tdp_blend, tdp_cond_blend and tdp_tile_mean, on ragged
+tdp_norm_filter, tdp_split_filter, tdp_blend, tdp_cond_blend, tdp_blend_cond and
+tdp_tile_mean, on ragged
 geometries (tails in every dimension, several batch items, minimal and odd
 channel counts).  Method: "Tiled Data Parallelism (TDP)" (LTX-2 docs, multigpu).
 """
@@ -170,6 +171,13 @@ def test_guard_bands(tdp, name, wl):
     torch.cuda.synchronize()
     _check_bands({"out": Rg}, "tdp_cond_blend")
     assert_blend_close(_host(Rg), oracle.cond_blend(p, Yc, ref["keep"], ref["idx"], ref["count"], ncap), wl)
+
+    # the post-model stage in one call: the same bytes as the two calls above
+    Zg2, Rg2 = _output((B, wl.F, wl.H, wl.W, C), lat), _output((B, N, C), lat)
+    tdp.tdp_blend_cond(plan, Yg.t, Zg2.t, N, ncap, Ycg.t, Sg.t, Rg2.t)
+    torch.cuda.synchronize()
+    _check_bands({"Z": Zg2, "out": Rg2}, "tdp_blend_cond")
+    assert np.array_equal(_host(Zg2), _host(Zg)) and np.array_equal(_host(Rg2), _host(Rg)), "tdp_blend_cond"
 
     # mean over tiles, a length that is not a multiple of the vector width
     L = 8 * 37 + 8
