@@ -194,7 +194,7 @@ def kernel_source_hash(names):
 
 _COMMON = ["tdp_device.cuh", "tdp_geom.h", "tdp_internal.h"]
 KERNEL_SOURCES = {
-    "tdp_blend_kernel": ["tdp_blend.cu"] + _COMMON,
+    "tdp_blend_kernel": ["tdp_blend.cu", "tdp_blend_row.cuh"] + _COMMON,
     "tdp_split_kernel": ["tdp_split.cu", "tdp_filter.cuh"] + _COMMON,
     "tdp_split_filter_kernel": ["tdp_split.cu", "tdp_filter.cuh"] + _COMMON,
     "tdp_split_tma_kernel": ["tdp_split_tma.cu"] + _COMMON,
