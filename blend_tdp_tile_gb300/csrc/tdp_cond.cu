@@ -93,7 +93,7 @@ tdp_cond_blend_kernel(const __grid_constant__ tdp_geom g, int32_t N, int32_t nca
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[e] += run[e];
         }
-        if (act) __stcs(out + tok * CV + cv, den > 0 ? acc_div<BF16>(acc, (float)den) : make_uint4(0u, 0u, 0u, 0u));
+        if (act) __stcs(out + tok * CV + cv, den > 0 ? acc_weigh<BF16>(acc, (float)den) : make_uint4(0u, 0u, 0u, 0u));
     }
 }
 
@@ -110,7 +110,7 @@ tdp_cond_blend_runs_kernel(const __grid_constant__ tdp_geom g, int32_t N, int32_
 
 // Block = kMeanVecs output vectors of out[B, L]; thread (part p, vector v) sums
 // tiles [p*nt/4, (p+1)*nt/4) in ascending order, kMeanUnroll loads in flight;
-// part 0 adds the four sums in order and divides.
+// part 0 adds the four sums in order and multiplies by the weight 1/nt.
 template <int BF16>
 __global__ void __launch_bounds__(kMeanVecs * kMeanParts)
 tdp_tile_mean_kernel(int32_t nt, int64_t nvec, const uint4 *__restrict__ A, uint4 *__restrict__ out)
@@ -141,7 +141,7 @@ tdp_tile_mean_kernel(int32_t nt, int64_t nvec, const uint4 *__restrict__ A, uint
         for (int q = 1; q < kMeanParts; ++q)
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[e] += s_part[q][e][vi];
-        __stcs(out + v, acc_div<BF16>(acc, (float)nt));
+        __stcs(out + v, acc_weigh<BF16>(acc, (float)nt));
     }
 }
 

@@ -12,8 +12,9 @@
 // another with no barrier in between, so a token kept by every tile (a negative-time
 // token) is spread over all groups.  A token with one run is written by the group that
 // summed it; the run sums of a token with more wait in shared memory and are added in
-// order once per chunk of runs.  fp32 accumulation; the result is divided by the number
-// of tiles that kept the token (slot >= 0), rows at slot >= ncap being absent.
+// order once per chunk of runs.  fp32 accumulation; the sum is multiplied by the token's
+// weight, 1/(number of tiles that kept it (slot >= 0)) rounded once to fp32, rows at
+// slot >= ncap being absent.
 #pragma once
 
 #include "tdp_device.cuh"
@@ -27,6 +28,8 @@ constexpr int kRunMinBlocks = 8;  // resident blocks per SM the run kernel is co
 constexpr int kRunRows = 8;       // rows per run: a token's kept rows are summed in runs of 8
 constexpr int kPartFloats = 4096; // shared-memory floats for the run sums of a chunk of runs
 
+// a += y, 4 fp32 or 8 bf16 values; a bf16 value is added to its fp32 sum in one
+// mixed-precision add (the bf16 value widened exactly, the sum rounded to nearest).
 template <int BF16>
 __device__ __forceinline__ void acc_add(float (&a)[8], const uint4 &y)
 {
@@ -34,8 +37,10 @@ __device__ __forceinline__ void acc_add(float (&a)[8], const uint4 &y)
     if (BF16) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            a[2 * i] += tdp_bf16_lo(w[i]);
-            a[2 * i + 1] += tdp_bf16_hi(w[i]);
+            unsigned short lo, hi;
+            asm("mov.b32 {%0, %1}, %2;" : "=h"(lo), "=h"(hi) : "r"(w[i]));
+            asm("add.rn.f32.bf16 %0, %1, %0;" : "+f"(a[2 * i]) : "h"(lo));
+            asm("add.rn.f32.bf16 %0, %1, %0;" : "+f"(a[2 * i + 1]) : "h"(hi));
         }
     } else {
 #pragma unroll
@@ -43,16 +48,16 @@ __device__ __forceinline__ void acc_add(float (&a)[8], const uint4 &y)
     }
 }
 
+// a x (1/n), the weight 1/n rounded to fp32 once, stored as 4 fp32 or 8 bf16 values.
 template <int BF16>
-__device__ __forceinline__ uint4 acc_div(const float (&a)[8], float n)
+__device__ __forceinline__ uint4 acc_weigh(const float (&a)[8], float n)
 {
+    const float r = __frcp_rn(n);
     if (BF16)
-        return make_uint4(tdp_pack_bf16x2(__fdiv_rn(a[0], n), __fdiv_rn(a[1], n)),
-                          tdp_pack_bf16x2(__fdiv_rn(a[2], n), __fdiv_rn(a[3], n)),
-                          tdp_pack_bf16x2(__fdiv_rn(a[4], n), __fdiv_rn(a[5], n)),
-                          tdp_pack_bf16x2(__fdiv_rn(a[6], n), __fdiv_rn(a[7], n)));
-    return make_uint4(__float_as_uint(__fdiv_rn(a[0], n)), __float_as_uint(__fdiv_rn(a[1], n)),
-                      __float_as_uint(__fdiv_rn(a[2], n)), __float_as_uint(__fdiv_rn(a[3], n)));
+        return make_uint4(tdp_pack_bf16x2(a[0] * r, a[1] * r), tdp_pack_bf16x2(a[2] * r, a[3] * r),
+                          tdp_pack_bf16x2(a[4] * r, a[5] * r), tdp_pack_bf16x2(a[6] * r, a[7] * r));
+    return make_uint4(__float_as_uint(a[0] * r), __float_as_uint(a[1] * r), __float_as_uint(a[2] * r),
+                      __float_as_uint(a[3] * r));
 }
 
 // Shared memory of the run kernel for nt tiles (dynamic; offsets in bytes):
@@ -94,6 +99,30 @@ __device__ __forceinline__ void run_rows(const uint32_t *rows, const uint4 *__re
         if (i0 + u < len) acc_add<BF16>(acc, y[u]);
 }
 
+// s_slot[t][j] (row stride kRunTok + 1) = slot of token k0 + j in tile t, for tiles up to
+// MAXT >= nt (-1 for tokens past N), by the whole block: thread (j, t0) loads tiles t0,
+// t0 + kRunThreads / kRunTok, ..., all its loads in flight before any is stored.
+template <int MAXT>
+__device__ __forceinline__ void stage_slots(const int32_t *__restrict__ slot, int32_t nt, int32_t B, int32_t N,
+                                            int32_t b, int32_t k0, int32_t *s_slot)
+{
+    constexpr int kStep = kRunThreads / kRunTok;   // tiles per pass of the block
+    constexpr int kPer = MAXT / kStep;             // loads per thread
+    const int32_t j = threadIdx.x % kRunTok, t0 = threadIdx.x / kRunTok;
+    const bool tok_ok = k0 + j < N;
+    int32_t v[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const int32_t t = t0 + u * kStep;
+        v[u] = t < nt && tok_ok ? __ldg(slot + ((int64_t)t * B + b) * N + k0 + j) : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const int32_t t = t0 + u * kStep;
+        if (t < nt) s_slot[t * (kRunTok + 1) + j] = v[u];
+    }
+}
+
 // Block `blk` = tokens k0 .. k0 + kRunTok - 1 of batch item b (blocks numbered batch item
 // after batch item), by the whole block with run_layout(nt).bytes of dynamic shared
 // memory at dsm.  Waits for the work before it in the stream before it reads.
@@ -117,25 +146,11 @@ __device__ __forceinline__ void cond_runs_block(const tdp_geom &g, int32_t N, in
     const int32_t nkb = (N + kRunTok - 1) / kRunTok;
     const int32_t b = blk / nkb, k0 = (blk - b * nkb) * kRunTok;
     const int32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    // slots of the block's tokens in every tile (each tile's are one coalesced read),
-    // all of a thread's loads in flight before any is stored
-    {
-        constexpr int kStep = kRunThreads / kRunTok;               // tiles per pass of the block
-        constexpr int kPer = kStageTiles / kStep;                  // loads per thread
-        const int32_t j = threadIdx.x % kRunTok, t0 = threadIdx.x / kRunTok;
-        const bool tok_ok = k0 + j < N;
-        int32_t v[kPer];
-#pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-            const int32_t t = t0 + u * kStep;
-            v[u] = t < nt && tok_ok ? __ldg(slot + ((int64_t)t * g.B + b) * N + k0 + j) : -1;
-        }
-#pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-            const int32_t t = t0 + u * kStep;
-            if (t < nt) s_slot[t * (kRunTok + 1) + j] = v[u];
-        }
-    }
+    // slots of the block's tokens in every tile (each tile's are one coalesced read)
+    if (nt <= kStageTiles / 2)
+        stage_slots<kStageTiles / 2>(slot, nt, g.B, N, b, k0, s_slot);
+    else
+        stage_slots<kStageTiles>(slot, nt, g.B, N, b, k0, s_slot);
     __syncthreads();
     // per token, the rows of the tiles that kept it, in ascending tile order
     for (int32_t j = warp; j < kRunTok; j += kRunThreads / 32) {
@@ -195,7 +210,7 @@ __device__ __forceinline__ void cond_runs_block(const tdp_geom &g, int32_t N, in
                 if (s_run0[j + 1] - s_run0[j] == 1) {
                     if (act)
                         __stcs(out + ((int64_t)b * N + k0 + j) * CV + cv,
-                               den > 0 ? acc_div<BF16>(part, (float)den) : make_uint4(0u, 0u, 0u, 0u));
+                               den > 0 ? acc_weigh<BF16>(part, (float)den) : make_uint4(0u, 0u, 0u, 0u));
                 } else {
 #pragma unroll
                     for (int x = 0; x < 8; ++x) s_part[(x * P + (u - c0)) * lpt + gl] = part[x];
@@ -216,7 +231,7 @@ __device__ __forceinline__ void cond_runs_block(const tdp_geom &g, int32_t N, in
                     for (int x = 0; x < 8; ++x) acc[x] += s_part[(x * P + (q - c0)) * lpt + gl];
                 }
                 if (re <= c1) {
-                    if (act) __stcs(out + ((int64_t)b * N + k0 + j) * CV + cv, acc_div<BF16>(acc, (float)s_den[j]));
+                    if (act) __stcs(out + ((int64_t)b * N + k0 + j) * CV + cv, acc_weigh<BF16>(acc, (float)s_den[j]));
                 } else {
                     float *cout = s_carry + (ci & 1) * 256;
 #pragma unroll

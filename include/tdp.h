@@ -256,8 +256,9 @@ tdp_status tdp_split_filter(tdp_plan_t plan, const void *X, const int32_t *P, co
  * out[b,k,:] = (1/n) * sum over the tiles t that kept token k of
  * Ycond[t,b,slot[t,b,k],:], n = number of those tiles (slot >= 0, i.e. kcount);
  * fp32 accumulation in ascending t, in runs of 8 consecutive stored rows whose
- * sums are added in order, one division per element by n, stored in the plan's
- * dtype.  A token that no tile kept gets 0.
+ * sums are added in order, then one multiplication per element by the weight 1/n
+ * (rounded once to fp32), stored in the plan's dtype.  A token that no tile kept
+ * gets 0.
  *
  *   N      conditioning tokens per batch item (>= 0).
  *   ncap   rows reserved per (tile, batch item) in Ycond (>= 1).  A tile that kept
@@ -297,9 +298,10 @@ tdp_status tdp_blend_cond(tdp_plan_t plan, const void *Yout, void *Z, int32_t N,
  *  averaged across tiles; the page warns that this average is context for the
  *  video tiles, not a meaningful audio output.)
  *
- * out[b,l] = (sum over t of A[t,b,l]) / n_tiles, fp32 accumulation: the tiles
+ * out[b,l] = (1/n_tiles) * sum over t of A[t,b,l], fp32 accumulation: the tiles
  * of each quarter of the tile range in ascending t, then the four quarters' sums
- * in order; stored in the plan's dtype.
+ * in order, times the weight 1/n_tiles rounded once to fp32; stored in the plan's
+ * dtype.
  *
  *   L    elements per batch item; L * sizeof(element) must be a multiple of 16.
  *   A    device [n_tiles, B, L] (plan dtype), read.
