@@ -1,24 +1,22 @@
 // tdp_cond.cu -- the two reductions over tiles besides the latent blend
 // ("Tiled Data Parallelism (TDP)"):
-//   tdp_cond_blend_runs_kernel, tdp_cond_blend_kernel
+//   tdp_cond_blend_rows_kernel, tdp_cond_blend_kernel
 //                          each conditioning token's per-tile outputs averaged
 //                          over the tiles that kept it ("Shared negative
 //                          (reference) positions": weight 1/(tiles that kept it));
 //   tdp_tile_mean_kernel   the audio latent averaged over all tiles ("What it
 //                          is": audio is processed on every tile and averaged).
 // Both are gather form and accumulate in fp32; no atomics, no scratch.  The
-// conditioning blend sums each token's rows in ascending tile order in runs of
-// kRunRows rows and adds the runs' sums in order; the tile mean adds the tiles of
-// each quarter of the tile range in ascending order and then the four quarters'
-// sums in order.
+// conditioning blend adds each token's rows in ascending tile order, one after
+// another; the tile mean adds the tiles of each quarter of the tile range in
+// ascending order and then the four quarters' sums in order.
 //
 // tdp_cond_blend has two kernels.  With at most kStageTiles tiles (and rows of
-// Ycond numbered below 2^32), tdp_cond_blend_runs_kernel runs the block routine of
-// tdp_cond_runs.cuh, kRunTok tokens per block.  With more tiles,
-// tdp_cond_blend_kernel gives each token a warp, which reads the token's slots 32
-// tiles at a time.
+// Ycond numbered below 2^32), tdp_cond_blend_rows_kernel runs the block routine of
+// tdp_cond_rows.cuh, kTok tokens per block.  With more tiles, tdp_cond_blend_kernel
+// gives each token a warp, which reads the token's slots 32 tiles at a time.
 #include "tdp.h"
-#include "tdp_cond_runs.cuh"
+#include "tdp_cond_rows.cuh"
 #include "tdp_device.cuh"
 #include "tdp_internal.h"
 
@@ -34,8 +32,7 @@ constexpr int kMeanUnroll = 8;    // tile loads a tile-mean thread keeps in flig
 // Warp = one conditioning token (b, k).  Per round of 32 tiles, lane l loads the
 // token's slot in tile t0 + l; a ballot gives the tiles that kept it, in
 // ascending order, and their rows (lanes across the channel vectors) are loaded
-// up to kRowsInFlight at a time and summed in that order in runs of kRunRows,
-// each run's sum added to the total when it is complete.
+// up to kRowsInFlight at a time and added to the sum in that order.
 constexpr int kRowsInFlight = 4;
 
 template <int BF16>
@@ -52,9 +49,7 @@ tdp_cond_blend_kernel(const __grid_constant__ tdp_geom g, int32_t N, int32_t nca
     for (int32_t cv0 = 0; cv0 < CV; cv0 += 32) {
         const int32_t cv = cv0 + lane;
         const bool act = cv < CV;
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // runs before the current one
-        float run[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // the current run of kRunRows rows
-        int32_t n = 0;                                       // stored rows summed so far
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         int32_t den = 0;                                     // tiles that kept the token
         for (int32_t t0 = 0; t0 < g.nt; t0 += 32) {
             const int32_t t = t0 + lane;
@@ -76,36 +71,23 @@ tdp_cond_blend_kernel(const __grid_constant__ tdp_geom g, int32_t N, int32_t nca
                     }
                 }
 #pragma unroll
-                for (int u = 0; u < kRowsInFlight; ++u) {
-                    if (u < got && act) acc_add<BF16>(run, y[u]);
-                    if (u < got && (n + u + 1) % kRunRows == 0) {       // a run is complete
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            acc[e] += run[e];
-                            run[e] = 0.f;
-                        }
-                    }
-                }
-                n += got;
+                for (int u = 0; u < kRowsInFlight; ++u)
+                    if (u < got && act) acc_add<BF16>(acc, y[u]);
             }
-        }
-        if (n % kRunRows != 0) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] += run[e];
         }
         if (act) __stcs(out + tok * CV + cv, den > 0 ? acc_weigh<BF16>(acc, (float)den) : make_uint4(0u, 0u, 0u, 0u));
     }
 }
 
-// Block = tokens k0 .. k0 + kRunTok - 1 of batch item b.
+// Block = tokens k0 .. k0 + kTok - 1 of batch item b.
 template <int BF16>
-__global__ void __launch_bounds__(kRunThreads, kRunMinBlocks)
-tdp_cond_blend_runs_kernel(const __grid_constant__ tdp_geom g, int32_t N, int32_t ncap, int32_t CV, int32_t lpt,
+__global__ void __launch_bounds__(kTokThreads, kTokMinBlocks)
+tdp_cond_blend_rows_kernel(const __grid_constant__ tdp_geom g, int32_t N, int32_t ncap, int32_t CV,
                            const uint4 *__restrict__ Ycond, const int32_t *__restrict__ slot,
                            uint4 *__restrict__ out)
 {
     extern __shared__ __align__(16) unsigned char dsm[];
-    cond_runs_block<BF16>(g, N, ncap, CV, lpt, Ycond, slot, out, blockIdx.x, dsm);
+    cond_rows_block<BF16>(g, N, ncap, CV, Ycond, slot, out, blockIdx.x, dsm);
 }
 
 // Block = kMeanVecs output vectors of out[B, L]; thread (part p, vector v) sums
@@ -163,16 +145,14 @@ extern "C" tdp_status tdp_cond_blend(tdp_plan_t plan, int32_t N, int32_t ncap, c
     uint4 *o = reinterpret_cast<uint4 *>(out);
     cudaError_t err;
     if (g.nt <= kStageTiles && (uint64_t)g.nt * (uint64_t)g.B * (uint64_t)ncap <= 0xffffffffull) {
-        const int64_t blocks = (int64_t)g.B * ((N + kRunTok - 1) / kRunTok);
+        const int64_t blocks = (int64_t)g.B * ((N + kTok - 1) / kTok);
         if (blocks > 0x7fffffffLL) return tdp_fail(TDP_ERR_TOO_LARGE, "cond blend grid too large");
-        int32_t lpt = 1;                                      // lanes per token: CV rounded up to 2^k, <= 32
-        while (lpt < CV && lpt < 32) lpt *= 2;
-        const size_t smem = run_layout(g.nt).bytes;
+        const size_t smem = rows_layout(g.nt).bytes;
         err = g.dtype == TDP_BF16
-                  ? tdp_launch_smem(true, tdp_cond_blend_runs_kernel<1>, (unsigned)blocks, kRunThreads, smem, s, g, N,
-                                    ncap, CV, lpt, y, slot, o)
-                  : tdp_launch_smem(true, tdp_cond_blend_runs_kernel<0>, (unsigned)blocks, kRunThreads, smem, s, g, N,
-                                    ncap, CV, lpt, y, slot, o);
+                  ? tdp_launch_smem(true, tdp_cond_blend_rows_kernel<1>, (unsigned)blocks, kTokThreads, smem, s, g, N,
+                                    ncap, CV, y, slot, o)
+                  : tdp_launch_smem(true, tdp_cond_blend_rows_kernel<0>, (unsigned)blocks, kTokThreads, smem, s, g, N,
+                                    ncap, CV, y, slot, o);
     } else {
         const int64_t warps = (int64_t)g.B * N;              // one warp per conditioning token
         const int64_t blocks = (warps + kThreads / 32 - 1) / (kThreads / 32);

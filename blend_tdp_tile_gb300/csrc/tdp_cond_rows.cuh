@@ -1,0 +1,231 @@
+// tdp_cond_rows.cuh -- the conditioning-token output reduction for up to kStageTiles
+// tiles ("Tiled Data Parallelism (TDP)", section "Shared negative (reference)
+// positions": a token kept by several tiles has blend weight 1/(number of tiles that
+// kept it)), as a block-level routine shared by tdp_cond_blend_rows_kernel and the fused
+// post-model kernel of tdp_blend_cond.
+//
+// A block takes kTok consecutive tokens of one batch item.
+//   1. Slots: the block stages the tokens' slots [tile][token] in shared memory, each
+//      tile's slots one coalesced read.
+//   2. Lists: a half-warp per token lists, in ascending tile order, the rows of Ycond of
+//      the tiles that kept the token (lane h looks at tiles u*16 + h; ballots rank the
+//      stored rows), counts the tiles that kept it, and the lists are packed into one flat
+//      list, token after token.
+//   3. Rows: the flat list's rows are copied into a ring of kStages shared-memory stages
+//      of kChunkRows rows with cp.async, the next stage in flight while one is summed; the
+//      copies of a stage are shared by all threads, so a token kept by every tile costs
+//      its half-warp no more copy work than any other.
+//   4. Sums: each token's half-warp adds its rows of every stage to its fp32 sums in list
+//      order, so a token's sum runs over its tiles in ascending order, one row after
+//      another, and does not depend on the tokens around it.  After the last stage the
+//      sum is multiplied by the token's weight, 1/(number of tiles that kept it
+//      (slot >= 0)) rounded once to fp32; rows at slot >= ncap are absent.
+#pragma once
+
+#include "tdp_device.cuh"
+
+namespace tdp_cr {
+
+constexpr int kStageTiles = 256;  // most tiles the routine handles
+constexpr int kTokThreads = 128;  // threads per token block
+constexpr int kTok = 8;           // tokens per block: a half-warp each
+constexpr int kLanes = 16;        // lanes per token: channel vectors per slab
+constexpr int kTokMinBlocks = 8;  // resident blocks per SM the token kernel is compiled for
+constexpr int kChunkRows = 48;    // rows per stage of the ring
+constexpr int kStages = 2;        // stages of the ring
+static_assert(kTokThreads == kTok * kLanes, "a half-warp per token");
+static_assert((kChunkRows * kLanes) % kTokThreads == 0, "the copies of a stage split evenly over the block");
+
+// a += y, 4 fp32 or 8 bf16 values; a bf16 value is added to its fp32 sum in one
+// mixed-precision add (the bf16 value widened exactly, the sum rounded to nearest).
+template <int BF16>
+__device__ __forceinline__ void acc_add(float (&a)[8], const uint4 &y)
+{
+    const uint32_t w[4] = {y.x, y.y, y.z, y.w};
+    if (BF16) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            unsigned short lo, hi;
+            asm("mov.b32 {%0, %1}, %2;" : "=h"(lo), "=h"(hi) : "r"(w[i]));
+            asm("add.rn.f32.bf16 %0, %1, %0;" : "+f"(a[2 * i]) : "h"(lo));
+            asm("add.rn.f32.bf16 %0, %1, %0;" : "+f"(a[2 * i + 1]) : "h"(hi));
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) a[i] += __uint_as_float(w[i]);
+    }
+}
+
+// a x (1/n), the weight 1/n rounded to fp32 once, stored as 4 fp32 or 8 bf16 values.
+template <int BF16>
+__device__ __forceinline__ uint4 acc_weigh(const float (&a)[8], float n)
+{
+    const float r = __frcp_rn(n);
+    if (BF16)
+        return make_uint4(tdp_pack_bf16x2(a[0] * r, a[1] * r), tdp_pack_bf16x2(a[2] * r, a[3] * r),
+                          tdp_pack_bf16x2(a[4] * r, a[5] * r), tdp_pack_bf16x2(a[6] * r, a[7] * r));
+    return make_uint4(__float_as_uint(a[0] * r), __float_as_uint(a[1] * r), __float_as_uint(a[2] * r),
+                      __float_as_uint(a[3] * r));
+}
+
+// 16-byte copy global -> shared (L2 only), and its group bookkeeping.
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem)
+{
+    const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Dynamic shared memory of the routine for nt tiles (offsets in bytes):
+//   ring  [kStages][kChunkRows][kLanes] uint4  row stages.  Before the rows it holds the
+//         staged slots [nt][kTok + 1] int32 (+1: a half-warp's column reads spread over
+//         the banks) and, past them, the per-token lists [kTok][nt] uint32.
+//   flat  [kTok * nt] uint32  the block's rows of Ycond, token after token, ascending tile
+//   len   [kTok] int32  stored rows per token
+struct rows_layout {
+    size_t flat, len, bytes;
+    __host__ __device__ constexpr explicit rows_layout(int32_t nt)
+        : flat((size_t)kStages * kChunkRows * kLanes * 16),
+          len(flat + (((size_t)kTok * nt * 4 + 15) & ~(size_t)15)),
+          bytes(len + kTok * 4)
+    {
+    }
+};
+static_assert(rows_layout(kStageTiles).bytes <= 48 * 1024, "token blocks must fit the default 48 KB of shared memory");
+static_assert((((size_t)kStageTiles * (kTok + 1) * 4 + 15) & ~(size_t)15) + (size_t)kStageTiles * kTok * 4 <=
+                  (size_t)kStages * kChunkRows * kLanes * 16,
+              "the staged slots and the per-token lists fit in the row ring");
+
+// s_slot[t][j] (row stride kTok + 1) = slot of token k0 + j in tile t, for tiles up to
+// MAXT >= nt (-1 for tokens past N), by the whole block: thread (j, t0) loads tiles t0,
+// t0 + kTokThreads / kTok, ..., each warp load covering 4 tiles x 8 tokens (4 whole
+// 32-byte sectors), all its loads in flight before any is stored.
+template <int MAXT>
+__device__ __forceinline__ void stage_slots(const int32_t *__restrict__ slot, int32_t nt, int32_t B, int32_t N,
+                                            int32_t b, int32_t k0, int32_t *s_slot)
+{
+    constexpr int kStep = kTokThreads / kTok;      // tiles per pass of the block
+    constexpr int kPer = MAXT / kStep;             // loads per thread
+    const int32_t j = threadIdx.x % kTok, t0 = threadIdx.x / kTok;
+    const bool tok_ok = k0 + j < N;
+    int32_t v[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const int32_t t = t0 + u * kStep;
+        v[u] = t < nt && tok_ok ? __ldg(slot + ((int64_t)t * B + b) * N + k0 + j) : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const int32_t t = t0 + u * kStep;
+        if (t < nt) s_slot[t * (kTok + 1) + j] = v[u];
+    }
+}
+
+// Block `blk` = tokens k0 .. k0 + kTok - 1 of batch item b (blocks numbered batch item
+// after batch item), by the whole block with rows_layout(nt).bytes of dynamic shared
+// memory at dsm.  Waits for the work before it in the stream before it reads.  The
+// caller guarantees nt <= kStageTiles and rows of Ycond numbered below 2^32.
+template <int BF16>
+__device__ __forceinline__ void cond_rows_block(const tdp_geom &g, int32_t N, int32_t ncap, int32_t CV,
+                                                const uint4 *__restrict__ Ycond, const int32_t *__restrict__ slot,
+                                                uint4 *__restrict__ out, int32_t blk, unsigned char *dsm)
+{
+    const int32_t nt = g.nt;
+    const rows_layout L(nt);
+    uint4 *s_ring = reinterpret_cast<uint4 *>(dsm);
+    int32_t *s_slot = reinterpret_cast<int32_t *>(dsm);
+    uint32_t *s_flat = reinterpret_cast<uint32_t *>(dsm + L.flat);
+    int32_t *s_len = reinterpret_cast<int32_t *>(dsm + L.len);
+    tdp_pdl_trigger();
+    tdp_pdl_wait();
+    const int32_t nkb = (N + kTok - 1) / kTok;
+    const int32_t b = blk / nkb, k0 = (blk - b * nkb) * kTok;
+    // 1. slots
+    if (nt <= kStageTiles / 2)
+        stage_slots<kStageTiles / 2>(slot, nt, g.B, N, b, k0, s_slot);
+    else
+        stage_slots<kStageTiles>(slot, nt, g.B, N, b, k0, s_slot);
+    __syncthreads();
+    // 2. lists: half-warp j, token k = k0 + j; lane h looks at tiles u*16 + h, so the
+    // token's stored rows come out in ascending tile order (u, then h)
+    const int32_t j = threadIdx.x / kLanes, h = threadIdx.x % kLanes;
+    const int32_t k = k0 + j;
+    const int32_t hs = threadIdx.x & 16;                      // this half's bits in a ballot
+    const uint32_t below = (1u << h) - 1u;
+    uint32_t *s_row = reinterpret_cast<uint32_t *>(dsm + (((size_t)nt * (kTok + 1) * 4 + 15) & ~(size_t)15)) + j * nt;
+    int32_t len = 0, den = 0;
+    for (int32_t t0 = 0; t0 < nt; t0 += kLanes) {
+        const int32_t t = t0 + h;
+        const int32_t sl = t < nt ? s_slot[t * (kTok + 1) + j] : -1;
+        const bool st = sl >= 0 && sl < ncap;
+        den += __popc((__ballot_sync(0xffffffffu, sl >= 0) >> hs) & 0xffffu);
+        const uint32_t hb = (__ballot_sync(0xffffffffu, st) >> hs) & 0xffffu;
+        if (st) s_row[len + __popc(hb & below)] = ((uint32_t)t * (uint32_t)g.B + (uint32_t)b) * (uint32_t)ncap + (uint32_t)sl;
+        len += __popc(hb);
+    }
+    if (h == 0) s_len[j] = len;
+    __syncthreads();
+    int32_t base = 0, R = 0;                                  // token j's place in the flat list; its length
+#pragma unroll
+    for (int q = 0; q < kTok; ++q) {
+        const int32_t lq = s_len[q];
+        base += q < j ? lq : 0;
+        R += lq;
+    }
+    for (int32_t i = h; i < len; i += kLanes) s_flat[base + i] = s_row[i];
+    __syncthreads();   // the flat list is complete; the ring is free for the rows
+    const int32_t nslab = (CV + kLanes - 1) / kLanes;
+    const bool tok_ok = k < N;
+    if (R == 0) {      // no stored row in the block: every output is 0
+        for (int32_t cv = h; cv < CV; cv += kLanes)
+            if (tok_ok) __stcs(out + ((int64_t)b * N + k) * CV + cv, make_uint4(0u, 0u, 0u, 0u));
+        return;
+    }
+    // 3. rows: units q = (slab of kLanes channel vectors, chunk of kChunkRows rows of the
+    // flat list), copied kStages - 1 units ahead of the one being summed
+    const int32_t nch = (R + kChunkRows - 1) / kChunkRows;
+    const int32_t nunit = nch * nslab;
+    auto issue = [&](int32_t q) {
+        if (q < nunit) {
+            const int32_t s = q / nch, c = q - s * nch;
+            uint4 *buf = s_ring + (q % kStages) * (kChunkRows * kLanes);
+#pragma unroll
+            for (int i = 0; i < kChunkRows * kLanes / kTokThreads; ++i) {
+                const int32_t e = threadIdx.x + i * kTokThreads;
+                const int32_t fi = c * kChunkRows + e / kLanes, cv = s * kLanes + e % kLanes;
+                if (fi < R && cv < CV) cp_async16(buf + e, Ycond + (uint64_t)s_flat[fi] * (uint32_t)CV + cv);
+            }
+        }
+        cp_async_commit();
+    };
+#pragma unroll
+    for (int q = 0; q < kStages - 1; ++q) issue(q);
+    // 4. sums: token j's rows of each unit, in list order
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int32_t q = 0; q < nunit; ++q) {
+        issue(q + kStages - 1);
+        cp_async_wait<kStages - 1>();
+        __syncthreads();                                      // unit q is in its stage for every thread
+        const int32_t s = q / nch, c = q - s * nch;
+        const int32_t cv = s * kLanes + h;
+        const uint4 *buf = s_ring + (q % kStages) * (kChunkRows * kLanes);
+        const int32_t i0 = max(base, c * kChunkRows), i1 = min(base + len, (c + 1) * kChunkRows);
+        if (cv < CV) {
+#pragma unroll 4
+            for (int32_t i = i0; i < i1; ++i) acc_add<BF16>(acc, buf[(i - c * kChunkRows) * kLanes + h]);
+        }
+        if (c == nch - 1) {                                   // the slab's last chunk: the output
+            if (tok_ok && cv < CV)
+                __stcs(out + ((int64_t)b * N + k) * CV + cv,
+                       den > 0 ? acc_weigh<BF16>(acc, (float)den) : make_uint4(0u, 0u, 0u, 0u));
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+        }
+        __syncthreads();                                      // the stage may be refilled
+    }
+    cp_async_wait<0>();
+}
+
+}  // namespace tdp_cr

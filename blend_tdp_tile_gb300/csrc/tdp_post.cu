@@ -5,8 +5,8 @@
 // 1/(number of tiles that kept it)).
 //
 // tdp_blend_cond_kernel is one grid of two kinds of block, both 128 threads: latent rows
-// (tdp_blend_row.cuh's blend_row) and conditioning-token blocks (tdp_cond_runs.cuh's
-// cond_runs_block).  The token blocks are latency-bound and the rows bandwidth-bound, so
+// (tdp_blend_row.cuh's blend_row) and conditioning-token blocks (tdp_cond_rows.cuh's
+// cond_rows_block).  The token blocks are latency-bound and the rows bandwidth-bound, so
 // the token blocks sit behind two device-fulls of rows in block order: they start once
 // the rows stream at full rate and run beside them instead of after them.  Every output
 // is bit for bit what tdp_blend and tdp_cond_blend write.
@@ -15,14 +15,14 @@
 
 #include "tdp.h"
 #include "tdp_blend_row.cuh"
-#include "tdp_cond_runs.cuh"
+#include "tdp_cond_rows.cuh"
 #include "tdp_internal.h"
 
 namespace {
 
 constexpr int kPostThreads = 128;
 constexpr int kPostMinBlocks = 6;
-static_assert(tdp_bl::kBlendThreads == kPostThreads && tdp_cr::kRunThreads == kPostThreads,
+static_assert(tdp_bl::kBlendThreads == kPostThreads && tdp_cr::kTokThreads == kPostThreads,
               "rows and token blocks share one launch");
 
 // Blocks [0, fpos): rows 0..fpos-1; [fpos, fpos + ncond): conditioning-token blocks;
@@ -30,14 +30,14 @@ static_assert(tdp_bl::kBlendThreads == kPostThreads && tdp_cr::kRunThreads == kP
 template <int BF16>
 __global__ void __launch_bounds__(kPostThreads, kPostMinBlocks)
 tdp_blend_cond_kernel(const __grid_constant__ tdp_geom g, int32_t cv_shift, const uint4 *__restrict__ Yout,
-                      uint4 *__restrict__ Z, int32_t N, int32_t ncap, int32_t CV, int32_t lpt,
+                      uint4 *__restrict__ Z, int32_t N, int32_t ncap, int32_t CV,
                       const uint4 *__restrict__ Ycond, const int32_t *__restrict__ slot, uint4 *__restrict__ outc,
                       int32_t fpos, int32_t ncond)
 {
     extern __shared__ __align__(16) unsigned char dsm[];
     const int32_t blk = blockIdx.x;
     if (blk >= fpos && blk < fpos + ncond) {
-        tdp_cr::cond_runs_block<BF16>(g, N, ncap, CV, lpt, Ycond, slot, outc, blk - fpos, dsm);
+        tdp_cr::cond_rows_block<BF16>(g, N, ncap, CV, Ycond, slot, outc, blk - fpos, dsm);
         return;
     }
     tdp_bl::blend_row<BF16>(g, cv_shift, Yout, Z, blk < fpos ? blk : blk - ncond, dsm);
@@ -89,13 +89,11 @@ extern "C" tdp_status tdp_blend_cond(tdp_plan_t plan, const void *Yout, void *Z,
         return st != TDP_OK ? st : tdp_cond_blend(plan, N, ncap, Ycond, slot, out, stream);
     }
     const int64_t rows = (int64_t)g.B * g.F * g.H;
-    const int64_t ncond = (int64_t)g.B * ((N + tdp_cr::kRunTok - 1) / tdp_cr::kRunTok);
+    const int64_t ncond = (int64_t)g.B * ((N + tdp_cr::kTok - 1) / tdp_cr::kTok);
     if (rows + ncond > 0x7fffffffLL) return tdp_fail(TDP_ERR_TOO_LARGE, "post-model grid too large");
     const int32_t CV = (g.C * g.esize) >> 4;
     const int32_t cv_shift = (CV & (CV - 1)) == 0 ? __builtin_ctz((unsigned)CV) : -1;
-    int32_t lpt = 1;                                          // lanes per token: CV rounded up to 2^k, <= 32
-    while (lpt < CV && lpt < 32) lpt *= 2;
-    const size_t smem = std::max(tdp_bl::blend_smem(g), tdp_cr::run_layout(g.nt).bytes);
+    const size_t smem = std::max(tdp_bl::blend_smem(g), tdp_cr::rows_layout(g.nt).bytes);
     cudaError_t err = cudaSuccess;
     const int64_t resident = g.dtype == TDP_BF16 ? prepare_post(tdp_blend_cond_kernel<1>, 1, smem, &err)
                                                  : prepare_post(tdp_blend_cond_kernel<0>, 0, smem, &err);
@@ -110,9 +108,9 @@ extern "C" tdp_status tdp_blend_cond(tdp_plan_t plan, const void *Yout, void *Z,
     uint4 *o = reinterpret_cast<uint4 *>(out);
     err = g.dtype == TDP_BF16
               ? tdp_launch_smem(true, tdp_blend_cond_kernel<1>, grid, kPostThreads, smem, s, g, cv_shift, y, z, N, ncap,
-                                CV, lpt, yc, slot, o, (int32_t)fpos, (int32_t)ncond)
+                                CV, yc, slot, o, (int32_t)fpos, (int32_t)ncond)
               : tdp_launch_smem(true, tdp_blend_cond_kernel<0>, grid, kPostThreads, smem, s, g, cv_shift, y, z, N, ncap,
-                                CV, lpt, yc, slot, o, (int32_t)fpos, (int32_t)ncond);
+                                CV, yc, slot, o, (int32_t)fpos, (int32_t)ncond);
     if (err == cudaSuccess) err = cudaGetLastError();
     if (err != cudaSuccess) return tdp_fail(TDP_ERR_CUDA, cudaGetErrorString(err));
     return tdp_ok();

@@ -255,10 +255,9 @@ tdp_status tdp_split_filter(tdp_plan_t plan, const void *X, const int32_t *P, co
  *
  * out[b,k,:] = (1/n) * sum over the tiles t that kept token k of
  * Ycond[t,b,slot[t,b,k],:], n = number of those tiles (slot >= 0, i.e. kcount);
- * fp32 accumulation in ascending t, in runs of 8 consecutive stored rows whose
- * sums are added in order, then one multiplication per element by the weight 1/n
- * (rounded once to fp32), stored in the plan's dtype.  A token that no tile kept
- * gets 0.
+ * one fp32 sum over those rows in ascending t, then one multiplication per element
+ * by the weight 1/n (rounded once to fp32), stored in the plan's dtype.  A token
+ * that no tile kept gets 0.
  *
  *   N      conditioning tokens per batch item (>= 0).
  *   ncap   rows reserved per (tile, batch item) in Ycond (>= 1).  A tile that kept

@@ -102,7 +102,7 @@ def test_cond_blend_ragged_tokens(tdp):
 
 
 def test_cond_blend_wide_channels(tdp):
-    """4 KB rows (bf16 C=2048): 256 vectors per token, more than one pass of lanes."""
+    """4 KB rows (bf16 C=2048): 256 vectors per token, sixteen slabs of 16 lanes."""
     wl = wk.by_name("tiny").replace(F=2, H=6, W=10, C=2048, dtype="bf16", num_tiles=(1, 2, 2),
                                     overlap=(0, 2, 2), n_cond=100)
     _cond_case(tdp, wl)
@@ -110,16 +110,17 @@ def test_cond_blend_wide_channels(tdp):
 
 @pytest.mark.parametrize("nw", [16, 17])
 def test_cond_blend_tile_count_edges(tdp, nw):
-    """256 tiles (the largest count the run kernel takes) and 272 (the warp-per-token kernel)."""
+    """256 tiles (the largest count the row kernel takes) and 272 (the warp-per-token kernel)."""
     wl = wk.by_name("tiny").replace(F=2, H=48, W=52, C=8, dtype="bf16", num_tiles=(1, 16, nw),
                                     overlap=(0, 1, 1), n_cond=200)
     _cond_case(tdp, wl)
 
 
-def test_cond_blend_runs_across_chunks(tdp):
-    """256 tiles and 1 KB rows (bf16 C=512: 64 vectors, two passes of 32 lanes): a token
-    kept by every tile has 32 runs of 8 rows, more than one chunk of run sums holds, so
-    its sum is carried from chunk to chunk; half the tokens have negative time."""
+def test_cond_blend_rows_across_stages(tdp):
+    """256 tiles and 1 KB rows (bf16 C=512: 64 vectors, four slabs of 16 lanes): a token
+    kept by every tile has 256 rows, more than five stages of the row ring, so its sum
+    continues from stage to stage and from slab to slab; half the tokens have negative
+    time."""
     wl = wk.by_name("tiny").replace(F=2, H=48, W=52, C=512, dtype="bf16", num_tiles=(1, 16, 16),
                                     overlap=(0, 1, 1), n_cond=120, neg_frac=0.5)
     out, _, _ = _cond_case(tdp, wl)
@@ -127,7 +128,8 @@ def test_cond_blend_runs_across_chunks(tdp):
 
 
 def test_cond_blend_odd_vector_count(tdp):
-    """bf16 C=136: 17 channel vectors, so 15 of a token's 32 lanes have no vector."""
+    """bf16 C=136: 17 channel vectors, two slabs, the second with one vector (15 of a
+    token's 16 lanes idle)."""
     wl = wk.by_name("tiny").replace(F=4, H=24, W=40, C=136, dtype="bf16", num_tiles=(2, 4, 8),
                                     overlap=(1, 2, 2), n_cond=400)
     _cond_case(tdp, wl)
