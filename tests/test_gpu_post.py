@@ -77,6 +77,12 @@ def test_fused_post_model_truncated_rows_and_no_tokens(tdp):
     assert _same(Z1, Z3)
 
 
+def test_fused_post_model_one_row_per_tile(tdp):
+    """ncap = 1: most token blocks hold no stored row and write only zeros."""
+    plan, out, Yout, Yc, ncap, Z1, O1, Z2, O2 = _case(tdp, wk.by_name("medium"), ncap=1)
+    assert _same(Z1, Z2) and _same(O1, O2)
+
+
 def test_fused_post_model_past_the_token_block_range(tdp):
     """2048 tiles: beyond the token-block routine, the call issues the two calls in turn."""
     wl = wk.by_name("tiny").replace(F=4, H=64, W=64, C=8, dtype="bf16", num_tiles=(2, 32, 32),

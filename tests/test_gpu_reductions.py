@@ -61,6 +61,16 @@ def test_cond_blend_truncated_rows(tdp):
     _cond_case(tdp, wk.by_name("small"), ncap=7)
 
 
+def test_cond_blend_one_row_per_tile(tdp):
+    """One row reserved per (tile, batch item): only each tile's first kept token is
+    stored, so most blocks of 8 tokens hold no stored row at all (their outputs are all
+    zero) while their tokens still carry the full 1/kcount weight."""
+    out, got, ref = _cond_case(tdp, wk.by_name("small").replace(B=2), ncap=1)
+    stored = (out["slot"] == 0).any(axis=0)                   # [B, N]: some tile stored the token
+    assert (~stored).sum() > 0.9 * stored.size
+    assert (as_f64(got)[~stored] == 0).all()
+
+
 def test_cond_blend_large_workload(tdp):
     _cond_case(tdp, wk.by_name("large"))
 
