@@ -123,6 +123,33 @@ __device__ __forceinline__ void stage_slots(const int32_t *__restrict__ slot, in
     }
 }
 
+// Token j's stored rows in ascending tile order into s_row[0 .. len), and the tiles that
+// kept it (den), by its half-warp: lane h looks at tiles u*16 + h, u < NU (NU*16 >= nt);
+// all of a lane's slot reads are issued before the ballots.
+template <int NU>
+__device__ __forceinline__ void list_rows(const int32_t *s_slot, int32_t nt, int32_t B, int32_t b, int32_t ncap,
+                                          int32_t j, int32_t h, uint32_t *s_row, int32_t &len, int32_t &den)
+{
+    const int32_t hs = threadIdx.x & 16;                      // this half's bits in a ballot
+    const uint32_t below = (1u << h) - 1u;
+    int32_t sl[NU];
+#pragma unroll
+    for (int u = 0; u < NU; ++u) {
+        const int32_t t = u * kLanes + h;
+        sl[u] = t < nt ? s_slot[t * (kTok + 1) + j] : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < NU; ++u) {
+        const bool st = sl[u] >= 0 && sl[u] < ncap;
+        den += __popc((__ballot_sync(0xffffffffu, sl[u] >= 0) >> hs) & 0xffffu);
+        const uint32_t hb = (__ballot_sync(0xffffffffu, st) >> hs) & 0xffffu;
+        if (st)
+            s_row[len + __popc(hb & below)] =
+                ((uint32_t)(u * kLanes + h) * (uint32_t)B + (uint32_t)b) * (uint32_t)ncap + (uint32_t)sl[u];
+        len += __popc(hb);
+    }
+}
+
 // Block `blk` = tokens k0 .. k0 + kTok - 1 of batch item b (blocks numbered batch item
 // after batch item), by the whole block with rows_layout(nt).bytes of dynamic shared
 // memory at dsm.  Waits for the work before it in the stream before it reads.  The
@@ -152,19 +179,12 @@ __device__ __forceinline__ void cond_rows_block(const tdp_geom &g, int32_t N, in
     // token's stored rows come out in ascending tile order (u, then h)
     const int32_t j = threadIdx.x / kLanes, h = threadIdx.x % kLanes;
     const int32_t k = k0 + j;
-    const int32_t hs = threadIdx.x & 16;                      // this half's bits in a ballot
-    const uint32_t below = (1u << h) - 1u;
     uint32_t *s_row = reinterpret_cast<uint32_t *>(dsm + (((size_t)nt * (kTok + 1) * 4 + 15) & ~(size_t)15)) + j * nt;
     int32_t len = 0, den = 0;
-    for (int32_t t0 = 0; t0 < nt; t0 += kLanes) {
-        const int32_t t = t0 + h;
-        const int32_t sl = t < nt ? s_slot[t * (kTok + 1) + j] : -1;
-        const bool st = sl >= 0 && sl < ncap;
-        den += __popc((__ballot_sync(0xffffffffu, sl >= 0) >> hs) & 0xffffu);
-        const uint32_t hb = (__ballot_sync(0xffffffffu, st) >> hs) & 0xffffu;
-        if (st) s_row[len + __popc(hb & below)] = ((uint32_t)t * (uint32_t)g.B + (uint32_t)b) * (uint32_t)ncap + (uint32_t)sl;
-        len += __popc(hb);
-    }
+    if (nt <= kStageTiles / 2)
+        list_rows<kStageTiles / 2 / kLanes>(s_slot, nt, g.B, b, ncap, j, h, s_row, len, den);
+    else
+        list_rows<kStageTiles / kLanes>(s_slot, nt, g.B, b, ncap, j, h, s_row, len, den);
     if (h == 0) s_len[j] = len;
     __syncthreads();
     int32_t base = 0, R = 0;                                  // token j's place in the flat list; its length
