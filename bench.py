@@ -787,8 +787,11 @@ def run_ours(args, rank, world, local_rank):
             per_workload[w.name] = {
                 "config": config_of(w, c.plan.total_tile_tokens, c.plan.n_tiles, "single GPU")["workload"],
                 "l2": "flushed before every launch" if fl is not None else "inputs larger than L2; no flush",
-                "calls": {k: {"ms": v["ms"], "GB/s": v["GB/s"], "frac": v["frac"],
-                              "frac_of_nominal_8tbs": v["frac_of_nominal_8tbs"]} for k, v in calls.items()},
+                "calls": {k: dict({"ms": v["ms"], "GB/s": v["GB/s"], "frac": v["frac"],
+                                   "frac_of_nominal_8tbs": v["frac_of_nominal_8tbs"]},
+                                  **({"traffic": profiled_traffic("tdp_" + k, w.name)}
+                                     if "tdp_" + k in CALL_KERNELS else {}))
+                          for k, v in calls.items()},
                 "latent_tokens_per_s": calls["step"]["latent_tokens_per_s"],
             }
             if c is not case:
