@@ -666,6 +666,22 @@ def run_ours(args, rank, world, local_rank):
         extras["launch_floor_ms"] = call_ms(torch, s, lambda: tiny.add_(1), reps, flush)
         del flush
         extras["cond_blend"]["shape"] = f"{plan.n_tiles} tiles x {ncap} rows x {wl.C} ch, {kept_rows} kept rows"
+        # the same reduction in two calls: the records made once (the conditioning tokens do
+        # not change between denoising steps), then each step's call from the records
+        if plan.n_tiles <= 256:
+            recs = torch.empty(tdp.tdp_cond_records_size(plan, N), dtype=torch.int32, device=dev)
+            flush = L2Flush(torch, dev)
+            rec_ms = call_ms(torch, s, lambda: tdp.tdp_cond_records(plan, N, ncap, slot2, recs, stream=s), 10, flush)
+            nblk = wl.B * ((N + 7) // 8)
+            rec_bytes = (kept_rows * wl.C * wl.esize + nblk * 18 * 4 + kept_rows * 4 + wl.B * N * wl.C * wl.esize)
+            extras["cond_blend_records"] = call_entry(
+                call_ms(torch, s, lambda: tdp.tdp_cond_blend_records(plan, N, recs, Yc, ncap, Oc, stream=s), reps,
+                        flush), rec_bytes, peak)
+            extras["cond_blend_records"].update({
+                "timing": f"mean of {reps} launches, each after an L2 flush",
+                "bytes": "kept rows + the records' headers and row numbers + out (the slots are not read)",
+                "records_ms": rec_ms, "records": "tdp_cond_records, once per set of conditioning tokens (mean of 10)"})
+            del flush, recs
         extras["tile_mean"]["shape"] = f"{plan.n_tiles} tiles x {AUDIO_TOKENS} audio tokens x {wl.C} ch (synthetic)"
 
     # ---- end to end, through the C ABI: every step copies its inputs (latent,

@@ -27,6 +27,7 @@ __all__ = [
     "TDP_OK", "TDP_F32", "TDP_BF16", "TDP_MAX_TILES_PER_DIM", "TdpError",
     "Plan", "tdp_plan_create", "tdp_plan_info", "tdp_plan_destroy",
     "tdp_pos_bounds", "tdp_split", "tdp_split_tma", "tdp_norm_filter", "tdp_split_filter", "tdp_blend", "tdp_cond_blend",
+    "tdp_cond_records_size", "tdp_cond_records", "tdp_cond_blend_records",
     "tdp_tile_mean", "tdp_blend_partial", "tdp_blend_store", "tdp_blend_cond",
     "tdp_balanced_tile_split", "tdp_tiles_for_size", "tdp_rank_tiles",
     "tdp_status_str", "tdp_last_error_detail",
@@ -79,6 +80,12 @@ def _load():
     lib.tdp_split_filter.restype = ctypes.c_int
     lib.tdp_cond_blend.argtypes = [vp, i32, i32, vp, vp, vp, vp]
     lib.tdp_cond_blend.restype = ctypes.c_int
+    lib.tdp_cond_records_size.argtypes = [vp, i32, i64p]
+    lib.tdp_cond_records_size.restype = ctypes.c_int
+    lib.tdp_cond_records.argtypes = [vp, i32, i32, vp, vp, vp]
+    lib.tdp_cond_records.restype = ctypes.c_int
+    lib.tdp_cond_blend_records.argtypes = [vp, i32, vp, vp, vp, vp]
+    lib.tdp_cond_blend_records.restype = ctypes.c_int
     lib.tdp_tile_mean.argtypes = [vp, ctypes.c_int64, vp, vp, vp]
     lib.tdp_tile_mean.restype = ctypes.c_int
     lib.tdp_blend.argtypes = [vp, vp, vp, vp]
@@ -390,6 +397,34 @@ def tdp_cond_blend(plan: Plan, N, ncap, Ycond, slot, out, stream=None):
     c.run(_lib.tdp_cond_blend, plan.handle, N, ncap, c.ptr(Ycond, "Ycond", nt * B * ncap * C, lat, 16),
           c.ptr(slot, "slot", nt * B * N, (torch.int32,), 4),
           c.ptr(out, "out", B * N * C, lat, 16), stream=stream)
+
+
+def tdp_cond_records_size(plan: Plan, N) -> int:
+    """int32 elements of the records tdp_cond_records writes for N conditioning tokens."""
+    n = ctypes.c_int64(0)
+    _check(_lib.tdp_cond_records_size(plan.handle, int(N), ctypes.byref(n)), "tdp_cond_records_size")
+    return n.value
+
+
+def tdp_cond_records(plan: Plan, N, ncap, slot, recs, stream=None):
+    """Once per set of conditioning tokens: every token block's record (rows and weights), in
+    launch order, into recs (int32, tdp_cond_records_size elements)."""
+    torch = _torch()
+    B, nt, N, ncap = plan.B, plan.n_tiles, int(N), int(ncap)
+    c = _Call("tdp_cond_records")
+    c.run(_lib.tdp_cond_records, plan.handle, N, ncap, c.ptr(slot, "slot", nt * B * N, (torch.int32,), 4),
+          c.ptr(recs, "recs", tdp_cond_records_size(plan, N), (torch.int32,), 16), stream=stream)
+
+
+def tdp_cond_blend_records(plan: Plan, N, recs, Ycond, ncap, out, stream=None):
+    """tdp_cond_blend from the records tdp_cond_records made (same plan, N, ncap and slot)."""
+    torch = _torch()
+    B, nt, C, N, ncap = plan.B, plan.n_tiles, plan.C, int(N), int(ncap)
+    lat = _latent_dtypes(plan)
+    c = _Call("tdp_cond_blend_records")
+    c.run(_lib.tdp_cond_blend_records, plan.handle, N,
+          c.ptr(recs, "recs", tdp_cond_records_size(plan, N), (torch.int32,), 16),
+          c.ptr(Ycond, "Ycond", nt * B * ncap * C, lat, 16), c.ptr(out, "out", B * N * C, lat, 16), stream=stream)
 
 
 def tdp_tile_mean(plan: Plan, L, A, out, stream=None):

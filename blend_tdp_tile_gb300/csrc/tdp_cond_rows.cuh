@@ -78,18 +78,28 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
+// A token block's record: what the rows and sums of its tokens need, in int32 units
+//   [0] block number   [1] R, its stored rows   [2, 2 + kTok) rows per token (len)
+//   [2 + kTok, 2 + 2 kTok) tiles that kept each token (den)
+//   [kRecHead, kRecHead + R) the rows of Ycond, token after token, each token's in
+//   ascending tile order (the flat list).
+// It lives in shared memory while a block works, and tdp_cond_records stores one per block
+// in global memory, rec_ints(nt) apart.
+constexpr int kRecHead = 2 + 2 * kTok;
+__host__ __device__ constexpr int64_t rec_ints(int32_t nt)
+{
+    return ((int64_t)kRecHead + (int64_t)kTok * nt + 3) & ~(int64_t)3;
+}
+
 // Dynamic shared memory of the routine for nt tiles (offsets in bytes):
 //   ring  [kStages][kChunkRows][kLanes] uint4  row stages.  Before the rows it holds the
 //         staged slots [nt][kTok + 1] int32 (+1: a half-warp's column reads spread over
 //         the banks) and, past them, the per-token lists [kTok][nt] uint32.
-//   flat  [kTok * nt] uint32  the block's rows of Ycond, token after token, ascending tile
-//   len   [kTok] int32  stored rows per token
+//   rec   [rec_ints(nt)] int32  the block's record
 struct rows_layout {
-    size_t flat, len, bytes;
+    size_t rec, bytes;
     __host__ __device__ constexpr explicit rows_layout(int32_t nt)
-        : flat((size_t)kStages * kChunkRows * kLanes * 16),
-          len(flat + (((size_t)kTok * nt * 4 + 15) & ~(size_t)15)),
-          bytes(len + kTok * 4)
+        : rec((size_t)kStages * kChunkRows * kLanes * 16), bytes(rec + (size_t)rec_ints(nt) * 4)
     {
     }
 };
@@ -150,25 +160,21 @@ __device__ __forceinline__ void list_rows(const int32_t *s_slot, int32_t nt, int
     }
 }
 
-// Block `blk` = tokens k0 .. k0 + kTok - 1 of batch item b (blocks numbered batch item
-// after batch item), by the whole block with rows_layout(nt).bytes of dynamic shared
-// memory at dsm.  Waits for the work before it in the stream before it reads.  The
-// caller guarantees nt <= kStageTiles and rows of Ycond numbered below 2^32.
-template <int BF16>
-__device__ __forceinline__ void cond_rows_block(const tdp_geom &g, int32_t N, int32_t ncap, int32_t CV,
-                                                const uint4 *__restrict__ Ycond, const int32_t *__restrict__ slot,
-                                                uint4 *__restrict__ out, int32_t blk, unsigned char *dsm)
+// Token j's place in its block's flat list (thread (j, h) = (threadIdx.x / kLanes,
+// threadIdx.x % kLanes)): its rows are flat[base, base + len); den tiles kept it; the block
+// has R rows in all.
+struct tok_rows {
+    int32_t len, den, base, R;
+};
+
+// The record of block blk (tokens k0 .. k0 + kTok - 1 of batch item b) from the slots, into
+// the record region `rec` of shared memory, by the whole block; ends with a barrier.
+__device__ __forceinline__ tok_rows rows_from_slots(const tdp_geom &g, int32_t N, int32_t ncap,
+                                                    const int32_t *__restrict__ slot, int32_t blk, int32_t b,
+                                                    int32_t k0, unsigned char *dsm, int32_t *rec)
 {
     const int32_t nt = g.nt;
-    const rows_layout L(nt);
-    uint4 *s_ring = reinterpret_cast<uint4 *>(dsm);
     int32_t *s_slot = reinterpret_cast<int32_t *>(dsm);
-    uint32_t *s_flat = reinterpret_cast<uint32_t *>(dsm + L.flat);
-    int32_t *s_len = reinterpret_cast<int32_t *>(dsm + L.len);
-    tdp_pdl_trigger();
-    tdp_pdl_wait();
-    const int32_t nkb = (N + kTok - 1) / kTok;
-    const int32_t b = blk / nkb, k0 = (blk - b * nkb) * kTok;
     // 1. slots
     if (nt <= kStageTiles / 2)
         stage_slots<kStageTiles / 2>(slot, nt, g.B, N, b, k0, s_slot);
@@ -178,24 +184,49 @@ __device__ __forceinline__ void cond_rows_block(const tdp_geom &g, int32_t N, in
     // 2. lists: half-warp j, token k = k0 + j; lane h looks at tiles u*16 + h, so the
     // token's stored rows come out in ascending tile order (u, then h)
     const int32_t j = threadIdx.x / kLanes, h = threadIdx.x % kLanes;
-    const int32_t k = k0 + j;
     uint32_t *s_row = reinterpret_cast<uint32_t *>(dsm + (((size_t)nt * (kTok + 1) * 4 + 15) & ~(size_t)15)) + j * nt;
-    int32_t len = 0, den = 0;
+    tok_rows tr;
+    tr.len = 0;
+    tr.den = 0;
     if (nt <= kStageTiles / 2)
-        list_rows<kStageTiles / 2 / kLanes>(s_slot, nt, g.B, b, ncap, j, h, s_row, len, den);
+        list_rows<kStageTiles / 2 / kLanes>(s_slot, nt, g.B, b, ncap, j, h, s_row, tr.len, tr.den);
     else
-        list_rows<kStageTiles / kLanes>(s_slot, nt, g.B, b, ncap, j, h, s_row, len, den);
-    if (h == 0) s_len[j] = len;
+        list_rows<kStageTiles / kLanes>(s_slot, nt, g.B, b, ncap, j, h, s_row, tr.len, tr.den);
+    if (h == 0) {
+        rec[2 + j] = tr.len;
+        rec[2 + kTok + j] = tr.den;
+    }
     __syncthreads();
-    int32_t base = 0, R = 0;                                  // token j's place in the flat list; its length
+    tr.base = 0;
+    tr.R = 0;
 #pragma unroll
     for (int q = 0; q < kTok; ++q) {
-        const int32_t lq = s_len[q];
-        base += q < j ? lq : 0;
-        R += lq;
+        const int32_t lq = rec[2 + q];
+        tr.base += q < j ? lq : 0;
+        tr.R += lq;
     }
-    for (int32_t i = h; i < len; i += kLanes) s_flat[base + i] = s_row[i];
-    __syncthreads();   // the flat list is complete; the ring is free for the rows
+    uint32_t *flat = reinterpret_cast<uint32_t *>(rec + kRecHead);
+    for (int32_t i = h; i < tr.len; i += kLanes) flat[tr.base + i] = s_row[i];
+    if (threadIdx.x == 0) {
+        rec[0] = blk;
+        rec[1] = tr.R;
+    }
+    __syncthreads();   // the record is complete; the ring is free for the rows
+    return tr;
+}
+
+// Rows and sums of block b, k0 from its record in shared memory (rec, with the flat list at
+// rec + kRecHead): the outputs of its tokens, by the whole block.
+template <int BF16>
+__device__ __forceinline__ void rows_sum(int32_t N, int32_t CV, const uint4 *__restrict__ Ycond,
+                                         uint4 *__restrict__ out, int32_t b, int32_t k0, const tok_rows &tr,
+                                         unsigned char *dsm, const int32_t *rec)
+{
+    uint4 *s_ring = reinterpret_cast<uint4 *>(dsm);
+    const uint32_t *s_flat = reinterpret_cast<const uint32_t *>(rec + kRecHead);
+    const int32_t h = threadIdx.x % kLanes;
+    const int32_t k = k0 + (int32_t)threadIdx.x / kLanes;
+    const int32_t R = tr.R, base = tr.base, len = tr.len;
     const int32_t nslab = (CV + kLanes - 1) / kLanes;
     const bool tok_ok = k < N;
     if (R == 0) {      // no stored row in the block: every output is 0
@@ -239,13 +270,31 @@ __device__ __forceinline__ void cond_rows_block(const tdp_geom &g, int32_t N, in
         if (c == nch - 1) {                                   // the slab's last chunk: the output
             if (tok_ok && cv < CV)
                 __stcs(out + ((int64_t)b * N + k) * CV + cv,
-                       den > 0 ? acc_weigh<BF16>(acc, (float)den) : make_uint4(0u, 0u, 0u, 0u));
+                       tr.den > 0 ? acc_weigh<BF16>(acc, (float)tr.den) : make_uint4(0u, 0u, 0u, 0u));
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[e] = 0.f;
         }
         __syncthreads();                                      // the stage may be refilled
     }
     cp_async_wait<0>();
+}
+
+// Block `blk` = tokens k0 .. k0 + kTok - 1 of batch item b (blocks numbered batch item
+// after batch item), by the whole block with rows_layout(nt).bytes of dynamic shared
+// memory at dsm.  Waits for the work before it in the stream before it reads.  The
+// caller guarantees nt <= kStageTiles and rows of Ycond numbered below 2^32.
+template <int BF16>
+__device__ __forceinline__ void cond_rows_block(const tdp_geom &g, int32_t N, int32_t ncap, int32_t CV,
+                                                const uint4 *__restrict__ Ycond, const int32_t *__restrict__ slot,
+                                                uint4 *__restrict__ out, int32_t blk, unsigned char *dsm)
+{
+    int32_t *rec = reinterpret_cast<int32_t *>(dsm + rows_layout(g.nt).rec);
+    tdp_pdl_trigger();
+    tdp_pdl_wait();
+    const int32_t nkb = (N + kTok - 1) / kTok;
+    const int32_t b = blk / nkb, k0 = (blk - b * nkb) * kTok;
+    const tok_rows tr = rows_from_slots(g, N, ncap, slot, blk, b, k0, dsm, rec);
+    rows_sum<BF16>(N, CV, Ycond, out, b, k0, tr, dsm, rec);
 }
 
 }  // namespace tdp_cr

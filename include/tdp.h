@@ -274,6 +274,39 @@ tdp_status tdp_cond_blend(tdp_plan_t plan, int32_t N, int32_t ncap, const void *
                           const int32_t *slot, void *out, tdp_stream_t stream);
 
 /*
+ * tdp_cond_records_size, tdp_cond_records, tdp_cond_blend_records -- tdp_cond_blend in two
+ * parts, for a caller whose conditioning tokens stay the same from call to call (the
+ * filter's slot, and so each token's rows, then do too; in a denoising loop, every step).
+ * ("Shared negative (reference) positions": a token kept by several tiles has blend weight
+ *  1/(number of tiles that kept it).)
+ *
+ * tdp_cond_records, once: for every block of 8 consecutive tokens of a batch item, its
+ * record: the rows of Ycond its tokens sum (each token's in ascending tile order), the rows
+ * per token and the tiles that kept each token.  The records are stored in launch order,
+ * the blocks with the most rows first, so that the longest blocks start first.
+ * tdp_cond_blend_records, each call: out as tdp_cond_blend writes it, bit for bit, from the
+ * records instead of the slots.
+ *
+ *   N, ncap, slot   as for tdp_cond_blend (slot from tdp_norm_filter or tdp_split_filter).
+ *   recs            device int32, tdp_cond_records_size(plan, N) ints, 16-byte aligned; written
+ *                   by tdp_cond_records, read by tdp_cond_blend_records.  Layout: G = B *
+ *                   ceil(N/8) records of rec = ceil4(18 + 8 * n_tiles) ints each, the i-th
+ *                   launched i-th ([0] token block g = b * ceil(N/8) + k0/8, [1] its rows R,
+ *                   [2..10) rows per token, [10..18) tiles that kept each token, [18..18+R)
+ *                   row numbers (t*B + b)*ncap + slot of Ycond), then G ints: each token
+ *                   block's launch position.
+ *   Ycond, out      as for tdp_cond_blend, with the ncap the records were made with.
+ * Records made for one plan, N, ncap and slot are valid only for those.  At most 256 tiles
+ * (TDP_ERR_TOO_LARGE beyond; tdp_cond_blend takes any count).  tdp_cond_records runs three
+ * kernels; tdp_cond_blend_records one.
+ */
+tdp_status tdp_cond_records_size(tdp_plan_t plan, int32_t N, int64_t *ints);
+tdp_status tdp_cond_records(tdp_plan_t plan, int32_t N, int32_t ncap, const int32_t *slot, int32_t *recs,
+                            tdp_stream_t stream);
+tdp_status tdp_cond_blend_records(tdp_plan_t plan, int32_t N, const int32_t *recs, const void *Ycond, void *out,
+                                  tdp_stream_t stream);
+
+/*
  * tdp_blend_cond -- the post-model stage in one call: tdp_blend and tdp_cond_blend with
  * the same arguments and bit-identical results, in one launch instead of two.
  * ("What it is": the blended tiles are summed into the final result; "Shared negative

@@ -1,0 +1,158 @@
+"""tdp_cond_records + tdp_cond_blend_records, the conditioning-token output reduction in two
+calls ("Tiled Data Parallelism (TDP)", "Shared negative (reference) positions": weight
+1/(tiles that kept it)): the outputs are bit for bit those of tdp_cond_blend, which the
+reduction tests compare with the CPU oracle; the records themselves are checked against the
+filter's slots and counts."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wk
+from gpu_path import assert_blend_close, fill_sentinel, run_split_filter, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+TOK = 8          # tokens per block
+HEAD = 2 + 2 * TOK
+STAGE_ROWS = 48  # rows per stage of the row ring: blocks are launched by stages filled, most first
+
+
+@pytest.fixture(scope="module")
+def tdp():
+    import __graft_entry__
+    __graft_entry__.build()
+    import blend_tdp_tile_gb300
+    return blend_tdp_tile_gb300
+
+
+def _storage(wl, shape, seed):
+    x = np.random.default_rng(seed).standard_normal(shape, dtype=np.float32)
+    return x if wl.dtype == "f32" else wk.f32_to_bf16_bits(x)
+
+
+def _setup(tdp, wl, ncap=None):
+    X, P, K = wk.make_inputs(wl)
+    plan = tdp.tdp_plan_create(wl.B, wl.F, wl.H, wl.W, wl.C, wl.dtype, wl.num_tiles, wl.overlap)
+    out = run_split_filter(tdp, plan, wl, X, P, K, fused=True)
+    N = K.shape[2]
+    ncap = max(1, int(out["count"].max())) if ncap is None else ncap
+    return plan, out, N, ncap
+
+
+def _blends(tdp, plan, wl, out, N, ncap, seeds=(11,)):
+    import torch
+    dt = torch.float32 if wl.dtype == "f32" else torch.bfloat16
+    n = tdp.tdp_cond_records_size(plan, N)
+    recs = torch.full((n,), -7, dtype=torch.int32, device="cuda")
+    tdp.tdp_cond_records(plan, N, ncap, out["slotd"], recs)
+    res = []
+    for seed in seeds:
+        Yc = to_dev(_storage(wl, (plan.n_tiles, wl.B, ncap, wl.C), seed))
+        O1 = fill_sentinel(torch.empty((wl.B, N, wl.C), dtype=dt, device="cuda"))
+        O2 = fill_sentinel(torch.empty((wl.B, N, wl.C), dtype=dt, device="cuda"))
+        tdp.tdp_cond_blend(plan, N, ncap, Yc, out["slotd"], O1)
+        tdp.tdp_cond_blend_records(plan, N, recs, Yc, ncap, O2)
+        torch.cuda.synchronize()
+        res.append((Yc, O1, O2))
+    return recs, res
+
+
+def _same(a, b):
+    import torch
+    return torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+
+
+def _check_records(plan, wl, out, N, ncap, recs):
+    """Every token block has one record, at its launch position; the records list the rows of
+    the filter's slots in ascending tile order, and the launch order is by stages filled."""
+    B, nt = wl.B, plan.n_tiles
+    nkb = (N + TOK - 1) // TOK
+    G = B * nkb
+    stride = (HEAD + TOK * nt + 3) // 4 * 4
+    r = recs.cpu().numpy()
+    pos = r[G * stride:]
+    assert sorted(pos.tolist()) == list(range(G))
+    slot = out["slot"]                                     # [nt, B, N]
+    kcount = out["kcount"]                                 # [B, N]
+    classes = []
+    for g in range(G):
+        rec = r[pos[g] * stride:(pos[g] + 1) * stride]
+        assert rec[0] == g
+        b, k0 = divmod(g, nkb)
+        k0 *= TOK
+        rows = []
+        for j in range(TOK):
+            k = k0 + j
+            if k < N:
+                stored = [(t * B + b) * ncap + slot[t, b, k] for t in range(nt) if 0 <= slot[t, b, k] < ncap]
+                assert rec[2 + j] == len(stored) and rec[2 + TOK + j] == kcount[b, k]
+            else:
+                stored = []
+                assert rec[2 + j] == 0 and rec[2 + TOK + j] == 0
+            rows += stored
+        assert rec[1] == len(rows)
+        assert rec[HEAD:HEAD + len(rows)].astype(np.uint32).tolist() == rows
+        classes.append((pos[g], min(7, (len(rows) + STAGE_ROWS - 1) // STAGE_ROWS)))
+    order = [c for _, c in sorted(classes)]
+    assert order == sorted(order, reverse=True), "launch order is not by stages filled, most first"
+
+
+@pytest.mark.parametrize("name", ["tiny", "small", "medium", "temporal", "large"])
+def test_records_match_the_slot_path(tdp, name):
+    wl = wk.by_name(name)
+    plan, out, N, ncap = _setup(tdp, wl)
+    recs, res = _blends(tdp, plan, wl, out, N, ncap)
+    for _, O1, O2 in res:
+        assert _same(O1, O2), "tdp_cond_blend_records differs from tdp_cond_blend"
+    if name in ("tiny", "small", "medium"):
+        _check_records(plan, wl, out, N, ncap, recs)
+
+
+@pytest.mark.parametrize("ncap", [1, 7])
+def test_records_with_rows_past_capacity(tdp, ncap):
+    wl = wk.by_name("small").replace(B=2, n_cond=1003)
+    plan, out, N, ncap = _setup(tdp, wl, ncap=ncap)
+    recs, res = _blends(tdp, plan, wl, out, N, ncap)
+    for _, O1, O2 in res:
+        assert _same(O1, O2)
+    _check_records(plan, wl, out, N, ncap, recs)
+
+
+def test_records_serve_many_calls(tdp):
+    """One set of records, three calls with different per-tile outputs (the denoising loop)."""
+    wl = wk.by_name("temporal")
+    plan, out, N, ncap = _setup(tdp, wl)
+    recs, res = _blends(tdp, plan, wl, out, N, ncap, seeds=(1, 2, 3))
+    for _, O1, O2 in res:
+        assert _same(O1, O2)
+
+
+def test_records_against_the_oracle(tdp):
+    wl = wk.by_name("small")
+    plan, out, N, ncap = _setup(tdp, wl)
+    recs, res = _blends(tdp, plan, wl, out, N, ncap)
+    Yc, _, O2 = res[0]
+    ref = oracle.cond_blend(oracle.problem_of(wl), to_host(Yc), out["keep"], out["idx"], out["count"], ncap)
+    assert_blend_close(to_host(O2), ref, wl)
+
+
+def test_records_wide_and_odd_channels(tdp):
+    """bf16 C=136 (17 channel vectors: two slabs) and fp32, with a token kept by every tile."""
+    for wl in (wk.by_name("tiny").replace(F=4, H=24, W=40, C=136, dtype="bf16", num_tiles=(2, 4, 8),
+                                          overlap=(1, 2, 2), n_cond=400),
+               wk.by_name("tiny").replace(n_cond=77)):
+        plan, out, N, ncap = _setup(tdp, wl)
+        recs, res = _blends(tdp, plan, wl, out, N, ncap)
+        for _, O1, O2 in res:
+            assert _same(O1, O2)
+
+
+def test_records_at_the_tile_limit(tdp):
+    """256 tiles (the most the records take), half the tokens with negative time."""
+    wl = wk.by_name("tiny").replace(F=2, H=48, W=52, C=512, dtype="bf16", num_tiles=(1, 16, 16),
+                                    overlap=(0, 1, 1), n_cond=120, neg_frac=0.5)
+    plan, out, N, ncap = _setup(tdp, wl)
+    assert plan.n_tiles == 256
+    recs, res = _blends(tdp, plan, wl, out, N, ncap)
+    for _, O1, O2 in res:
+        assert _same(O1, O2)
