@@ -24,7 +24,9 @@ using namespace tdp_cr;
 
 constexpr int kOrderThreads = 1024;
 constexpr int kClasses = 8;        // launch classes: ring stages the rows fill, 7 or more in class 7
-constexpr int kFirstInts = 2 * kTokThreads;   // record ints a block reads before it knows R
+constexpr int kFirstInts = 4 * kTokThreads;   // record ints a block reads before it knows R (one int4 a thread)
+constexpr int kRecRows = 64;                  // rows per ring stage of the per-call kernel on plans of
+constexpr int kRecRowsTiles = 64;             // kRecRowsTiles tiles or more (tokens hold more rows), else kChunkRows
 
 __device__ __forceinline__ int32_t launch_class(int32_t R)
 {
@@ -116,24 +118,21 @@ tdp_cond_record_kernel(const __grid_constant__ tdp_geom g, int32_t N, int32_t nc
 
 // Block i = the token block whose record is the i-th: the record's first kFirstInts ints
 // (header and first rows) in one load per thread, the rest once R is known, then the rows
-// and sums of tdp_cond_rows.cuh.
-template <int BF16>
+// and sums of tdp_cond_rows.cuh through a ring of stages of CR rows.
+template <int BF16, int CR>
 __global__ void __launch_bounds__(kTokThreads, kTokMinBlocks)
 tdp_cond_blend_rec_kernel(int32_t nt, int32_t N, int32_t CV, const int32_t *__restrict__ recs,
                           const uint4 *__restrict__ Ycond, uint4 *__restrict__ out)
 {
     extern __shared__ __align__(16) unsigned char dsm[];
-    int32_t *rec = reinterpret_cast<int32_t *>(dsm + rows_layout(nt).rec);
+    int32_t *rec = reinterpret_cast<int32_t *>(dsm + rows_layout(nt, CR).rec);
     tdp_pdl_trigger();
     tdp_pdl_wait();
     const int64_t stride = rec_ints(nt);
     const int32_t *src = recs + (int64_t)blockIdx.x * stride;
     const int32_t first = stride < kFirstInts ? (int32_t)stride : kFirstInts;   // both multiples of 4
-    if (2 * (int32_t)threadIdx.x < first) {
-        const int2 v = __ldg(reinterpret_cast<const int2 *>(src) + threadIdx.x);
-        rec[2 * threadIdx.x] = v.x;
-        rec[2 * threadIdx.x + 1] = v.y;
-    }
+    if (4 * (int32_t)threadIdx.x < first)
+        reinterpret_cast<int4 *>(rec)[threadIdx.x] = __ldg(reinterpret_cast<const int4 *>(src) + threadIdx.x);
     __syncthreads();
     const int32_t blk = rec[0];
     tok_rows tr;
@@ -148,7 +147,7 @@ tdp_cond_blend_rec_kernel(int32_t nt, int32_t N, int32_t CV, const int32_t *__re
     __syncthreads();                                      // the whole record is in shared memory
     const int32_t nkb = (N + kTok - 1) / kTok;
     const int32_t b = blk / nkb, k0 = (blk - b * nkb) * kTok;
-    rows_sum<BF16>(N, CV, Ycond, out, b, k0, tr, dsm, rec);
+    rows_sum<BF16, CR>(N, CV, Ycond, out, b, k0, tr, dsm, rec);
 }
 
 // Token blocks of a problem and its record layout; TDP_OK when the records apply.
@@ -215,15 +214,25 @@ extern "C" tdp_status tdp_cond_blend_records(tdp_plan_t plan, int32_t N, const i
     if (!tdp_aligned(recs, 16) || !tdp_aligned(Ycond, 16) || !tdp_aligned(out, 16))
         return tdp_fail(TDP_ERR_MISALIGNED, "recs, Ycond and out need 16-byte alignment");
     const int32_t CV = (g.C * g.esize) >> 4;
-    const size_t smem = rows_layout(g.nt).bytes;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const uint4 *y = reinterpret_cast<const uint4 *>(Ycond);
     uint4 *o = reinterpret_cast<uint4 *>(out);
-    cudaError_t err = g.dtype == TDP_BF16
-                          ? tdp_launch_smem(true, tdp_cond_blend_rec_kernel<1>, (unsigned)G, kTokThreads, smem, s,
-                                            g.nt, N, CV, recs, y, o)
-                          : tdp_launch_smem(true, tdp_cond_blend_rec_kernel<0>, (unsigned)G, kTokThreads, smem, s,
-                                            g.nt, N, CV, recs, y, o);
+    cudaError_t err;
+    if (g.nt >= kRecRowsTiles) {
+        const size_t smem = rows_layout(g.nt, kRecRows).bytes;
+        err = g.dtype == TDP_BF16
+                  ? tdp_launch_smem(true, tdp_cond_blend_rec_kernel<1, kRecRows>, (unsigned)G, kTokThreads, smem, s,
+                                    g.nt, N, CV, recs, y, o)
+                  : tdp_launch_smem(true, tdp_cond_blend_rec_kernel<0, kRecRows>, (unsigned)G, kTokThreads, smem, s,
+                                    g.nt, N, CV, recs, y, o);
+    } else {
+        const size_t smem = rows_layout(g.nt).bytes;
+        err = g.dtype == TDP_BF16
+                  ? tdp_launch_smem(true, tdp_cond_blend_rec_kernel<1, kChunkRows>, (unsigned)G, kTokThreads, smem, s,
+                                    g.nt, N, CV, recs, y, o)
+                  : tdp_launch_smem(true, tdp_cond_blend_rec_kernel<0, kChunkRows>, (unsigned)G, kTokThreads, smem, s,
+                                    g.nt, N, CV, recs, y, o);
+    }
     if (err == cudaSuccess) err = cudaGetLastError();
     if (err != cudaSuccess) return tdp_fail(TDP_ERR_CUDA, cudaGetErrorString(err));
     return tdp_ok();

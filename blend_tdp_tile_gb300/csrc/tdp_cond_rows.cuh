@@ -31,10 +31,13 @@ constexpr int kTokThreads = 128;  // threads per token block
 constexpr int kTok = 8;           // tokens per block: a half-warp each
 constexpr int kLanes = 16;        // lanes per token: channel vectors per slab
 constexpr int kTokMinBlocks = 8;  // resident blocks per SM the token kernel is compiled for
-constexpr int kChunkRows = 48;    // rows per stage of the ring
+constexpr int kChunkRows = 48;    // rows per stage of the ring (the slot path's ring)
 constexpr int kStages = 2;        // stages of the ring
 static_assert(kTokThreads == kTok * kLanes, "a half-warp per token");
 static_assert((kChunkRows * kLanes) % kTokThreads == 0, "the copies of a stage split evenly over the block");
+
+// Bytes of a ring of kStages stages of CR rows.
+__host__ __device__ constexpr size_t ring_bytes(int CR) { return (size_t)kStages * CR * kLanes * 16; }
 
 // a += y, 4 fp32 or 8 bf16 values; a bf16 value is added to its fp32 sum in one
 // mixed-precision add (the bf16 value widened exactly, the sum rounded to nearest).
@@ -91,15 +94,15 @@ __host__ __device__ constexpr int64_t rec_ints(int32_t nt)
     return ((int64_t)kRecHead + (int64_t)kTok * nt + 3) & ~(int64_t)3;
 }
 
-// Dynamic shared memory of the routine for nt tiles (offsets in bytes):
-//   ring  [kStages][kChunkRows][kLanes] uint4  row stages.  Before the rows it holds the
-//         staged slots [nt][kTok + 1] int32 (+1: a half-warp's column reads spread over
-//         the banks) and, past them, the per-token lists [kTok][nt] uint32.
+// Dynamic shared memory of the routine for nt tiles and stages of CR rows (offsets in bytes):
+//   ring  [kStages][CR][kLanes] uint4  row stages.  Before the rows, on the slot path, it
+//         holds the staged slots [nt][kTok + 1] int32 (+1: a half-warp's column reads spread
+//         over the banks) and, past them, the per-token lists [kTok][nt] uint32.
 //   rec   [rec_ints(nt)] int32  the block's record
 struct rows_layout {
     size_t rec, bytes;
-    __host__ __device__ constexpr explicit rows_layout(int32_t nt)
-        : rec((size_t)kStages * kChunkRows * kLanes * 16), bytes(rec + (size_t)rec_ints(nt) * 4)
+    __host__ __device__ constexpr explicit rows_layout(int32_t nt, int CR = kChunkRows)
+        : rec(ring_bytes(CR)), bytes(rec + (size_t)rec_ints(nt) * 4)
     {
     }
 };
@@ -216,8 +219,9 @@ __device__ __forceinline__ tok_rows rows_from_slots(const tdp_geom &g, int32_t N
 }
 
 // Rows and sums of block b, k0 from its record in shared memory (rec, with the flat list at
-// rec + kRecHead): the outputs of its tokens, by the whole block.
-template <int BF16>
+// rec + kRecHead), through a ring of stages of CR rows at dsm: the outputs of its tokens, by
+// the whole block.
+template <int BF16, int CR = kChunkRows>
 __device__ __forceinline__ void rows_sum(int32_t N, int32_t CV, const uint4 *__restrict__ Ycond,
                                          uint4 *__restrict__ out, int32_t b, int32_t k0, const tok_rows &tr,
                                          unsigned char *dsm, const int32_t *rec)
@@ -227,6 +231,7 @@ __device__ __forceinline__ void rows_sum(int32_t N, int32_t CV, const uint4 *__r
     const int32_t h = threadIdx.x % kLanes;
     const int32_t k = k0 + (int32_t)threadIdx.x / kLanes;
     const int32_t R = tr.R, base = tr.base, len = tr.len;
+    static_assert((CR * kLanes) % kTokThreads == 0, "the copies of a stage split evenly over the block");
     const int32_t nslab = (CV + kLanes - 1) / kLanes;
     const bool tok_ok = k < N;
     if (R == 0) {      // no stored row in the block: every output is 0
@@ -234,18 +239,18 @@ __device__ __forceinline__ void rows_sum(int32_t N, int32_t CV, const uint4 *__r
             if (tok_ok) __stcs(out + ((int64_t)b * N + k) * CV + cv, make_uint4(0u, 0u, 0u, 0u));
         return;
     }
-    // 3. rows: units q = (slab of kLanes channel vectors, chunk of kChunkRows rows of the
+    // 3. rows: units q = (slab of kLanes channel vectors, chunk of CR rows of the
     // flat list), copied kStages - 1 units ahead of the one being summed
-    const int32_t nch = (R + kChunkRows - 1) / kChunkRows;
+    const int32_t nch = (R + CR - 1) / CR;
     const int32_t nunit = nch * nslab;
     auto issue = [&](int32_t q) {
         if (q < nunit) {
             const int32_t s = q / nch, c = q - s * nch;
-            uint4 *buf = s_ring + (q % kStages) * (kChunkRows * kLanes);
+            uint4 *buf = s_ring + (q % kStages) * (CR * kLanes);
 #pragma unroll
-            for (int i = 0; i < kChunkRows * kLanes / kTokThreads; ++i) {
+            for (int i = 0; i < CR * kLanes / kTokThreads; ++i) {
                 const int32_t e = threadIdx.x + i * kTokThreads;
-                const int32_t fi = c * kChunkRows + e / kLanes, cv = s * kLanes + e % kLanes;
+                const int32_t fi = c * CR + e / kLanes, cv = s * kLanes + e % kLanes;
                 if (fi < R && cv < CV) cp_async16(buf + e, Ycond + (uint64_t)s_flat[fi] * (uint32_t)CV + cv);
             }
         }
@@ -261,11 +266,11 @@ __device__ __forceinline__ void rows_sum(int32_t N, int32_t CV, const uint4 *__r
         __syncthreads();                                      // unit q is in its stage for every thread
         const int32_t s = q / nch, c = q - s * nch;
         const int32_t cv = s * kLanes + h;
-        const uint4 *buf = s_ring + (q % kStages) * (kChunkRows * kLanes);
-        const int32_t i0 = max(base, c * kChunkRows), i1 = min(base + len, (c + 1) * kChunkRows);
+        const uint4 *buf = s_ring + (q % kStages) * (CR * kLanes);
+        const int32_t i0 = max(base, c * CR), i1 = min(base + len, (c + 1) * CR);
         if (cv < CV) {
 #pragma unroll 4
-            for (int32_t i = i0; i < i1; ++i) acc_add<BF16>(acc, buf[(i - c * kChunkRows) * kLanes + h]);
+            for (int32_t i = i0; i < i1; ++i) acc_add<BF16>(acc, buf[(i - c * CR) * kLanes + h]);
         }
         if (c == nch - 1) {                                   // the slab's last chunk: the output
             if (tok_ok && cv < CV)
