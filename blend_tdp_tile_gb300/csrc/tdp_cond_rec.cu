@@ -24,9 +24,6 @@ using namespace tdp_cr;
 
 constexpr int kOrderThreads = 1024;
 constexpr int kClasses = 8;        // launch classes: ring stages the rows fill, 7 or more in class 7
-constexpr int kFirstInts = 4 * kTokThreads;   // record ints a block reads before it knows R (one int4 a thread)
-constexpr int kRecRows = 64;                  // rows per ring stage of the per-call kernel on plans of
-constexpr int kRecRowsTiles = 64;             // kRecRowsTiles tiles or more (tokens hold more rows), else kChunkRows
 
 __device__ __forceinline__ int32_t launch_class(int32_t R)
 {
@@ -116,38 +113,14 @@ tdp_cond_record_kernel(const __grid_constant__ tdp_geom g, int32_t N, int32_t nc
     for (int32_t i = threadIdx.x; i < kRecHead + tr.R; i += kTokThreads) dst[i] = rec[i];
 }
 
-// Block i = the token block whose record is the i-th: the record's first kFirstInts ints
-// (header and first rows) in one load per thread, the rest once R is known, then the rows
-// and sums of tdp_cond_rows.cuh through a ring of stages of CR rows.
+// Block i = the token block whose record is the i-th (tdp_cond_rows.cuh's cond_record_block).
 template <int BF16, int CR>
 __global__ void __launch_bounds__(kTokThreads, kTokMinBlocks)
 tdp_cond_blend_rec_kernel(int32_t nt, int32_t N, int32_t CV, const int32_t *__restrict__ recs,
                           const uint4 *__restrict__ Ycond, uint4 *__restrict__ out)
 {
     extern __shared__ __align__(16) unsigned char dsm[];
-    int32_t *rec = reinterpret_cast<int32_t *>(dsm + rows_layout(nt, CR).rec);
-    tdp_pdl_trigger();
-    tdp_pdl_wait();
-    const int64_t stride = rec_ints(nt);
-    const int32_t *src = recs + (int64_t)blockIdx.x * stride;
-    const int32_t first = stride < kFirstInts ? (int32_t)stride : kFirstInts;   // both multiples of 4
-    if (4 * (int32_t)threadIdx.x < first)
-        reinterpret_cast<int4 *>(rec)[threadIdx.x] = __ldg(reinterpret_cast<const int4 *>(src) + threadIdx.x);
-    __syncthreads();
-    const int32_t blk = rec[0];
-    tok_rows tr;
-    tr.R = rec[1];
-    for (int32_t i = first + (int32_t)threadIdx.x; i < kRecHead + tr.R; i += kTokThreads) rec[i] = __ldg(src + i);
-    const int32_t j = threadIdx.x / kLanes;
-    tr.len = rec[2 + j];
-    tr.den = rec[2 + kTok + j];
-    tr.base = 0;
-#pragma unroll
-    for (int q = 0; q < kTok; ++q) tr.base += q < j ? rec[2 + q] : 0;
-    __syncthreads();                                      // the whole record is in shared memory
-    const int32_t nkb = (N + kTok - 1) / kTok;
-    const int32_t b = blk / nkb, k0 = (blk - b * nkb) * kTok;
-    rows_sum<BF16, CR>(N, CV, Ycond, out, b, k0, tr, dsm, rec);
+    cond_record_block<BF16, CR>(nt, N, CV, recs, Ycond, out, blockIdx.x, dsm);
 }
 
 // Token blocks of a problem and its record layout; TDP_OK when the records apply.

@@ -39,6 +39,11 @@ static_assert((kChunkRows * kLanes) % kTokThreads == 0, "the copies of a stage s
 // Bytes of a ring of kStages stages of CR rows.
 __host__ __device__ constexpr size_t ring_bytes(int CR) { return (size_t)kStages * CR * kLanes * 16; }
 
+// The records path (tdp_cond_records) runs its blocks with stages of kRecRows rows on plans of
+// kRecRowsTiles tiles or more, where tokens hold more rows, else of kChunkRows.
+constexpr int kRecRows = 64;
+constexpr int kRecRowsTiles = 64;
+
 // a += y, 4 fp32 or 8 bf16 values; a bf16 value is added to its fp32 sum in one
 // mixed-precision add (the bf16 value widened exactly, the sum rounded to nearest).
 template <int BF16>
@@ -282,6 +287,52 @@ __device__ __forceinline__ void rows_sum(int32_t N, int32_t CV, const uint4 *__r
         __syncthreads();                                      // the stage may be refilled
     }
     cp_async_wait<0>();
+}
+
+// Record number i of the records tdp_cond_records stores (rec_ints(nt) ints apart from
+// recs) into the record region `rec` of shared memory, by the whole block: its first
+// kFirstInts ints (header and first rows) in one 16-byte load per thread, the rest once R is
+// known; *blk receives its token block.  Ends with a barrier.
+constexpr int kFirstInts = 4 * kTokThreads;
+__device__ __forceinline__ tok_rows rows_from_record(int32_t nt, const int32_t *__restrict__ recs, int32_t i,
+                                                     int32_t *rec, int32_t *blk)
+{
+    const int64_t stride = rec_ints(nt);
+    const int32_t *src = recs + (int64_t)i * stride;
+    const int32_t first = stride < kFirstInts ? (int32_t)stride : kFirstInts;   // both multiples of 4
+    if (4 * (int32_t)threadIdx.x < first)
+        reinterpret_cast<int4 *>(rec)[threadIdx.x] = __ldg(reinterpret_cast<const int4 *>(src) + threadIdx.x);
+    __syncthreads();
+    *blk = rec[0];
+    tok_rows tr;
+    tr.R = rec[1];
+    for (int32_t e = first + (int32_t)threadIdx.x; e < kRecHead + tr.R; e += kTokThreads) rec[e] = __ldg(src + e);
+    const int32_t j = threadIdx.x / kLanes;
+    tr.len = rec[2 + j];
+    tr.den = rec[2 + kTok + j];
+    tr.base = 0;
+#pragma unroll
+    for (int q = 0; q < kTok; ++q) tr.base += q < j ? rec[2 + q] : 0;
+    __syncthreads();                                      // the whole record is in shared memory
+    return tr;
+}
+
+// Block i of the per-call records path: the token block of record i, through a ring of
+// stages of CR rows (rows_layout(nt, CR).bytes of dynamic shared memory at dsm).  Waits for
+// the work before it in the stream before it reads.
+template <int BF16, int CR>
+__device__ __forceinline__ void cond_record_block(int32_t nt, int32_t N, int32_t CV, const int32_t *__restrict__ recs,
+                                                  const uint4 *__restrict__ Ycond, uint4 *__restrict__ out, int32_t i,
+                                                  unsigned char *dsm)
+{
+    int32_t *rec = reinterpret_cast<int32_t *>(dsm + rows_layout(nt, CR).rec);
+    tdp_pdl_trigger();
+    tdp_pdl_wait();
+    int32_t blk = 0;
+    const tok_rows tr = rows_from_record(nt, recs, i, rec, &blk);
+    const int32_t nkb = (N + kTok - 1) / kTok;
+    const int32_t b = blk / nkb, k0 = (blk - b * nkb) * kTok;
+    rows_sum<BF16, CR>(N, CV, Ycond, out, b, k0, tr, dsm, rec);
 }
 
 // Block `blk` = tokens k0 .. k0 + kTok - 1 of batch item b (blocks numbered batch item

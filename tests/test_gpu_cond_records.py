@@ -156,3 +156,4 @@ def test_records_at_the_tile_limit(tdp):
     recs, res = _blends(tdp, plan, wl, out, N, ncap)
     for _, O1, O2 in res:
         assert _same(O1, O2)
+
