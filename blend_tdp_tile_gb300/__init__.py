@@ -84,7 +84,7 @@ def _load():
     lib.tdp_cond_records_size.restype = ctypes.c_int
     lib.tdp_cond_records.argtypes = [vp, i32, i32, vp, vp, vp]
     lib.tdp_cond_records.restype = ctypes.c_int
-    lib.tdp_cond_blend_records.argtypes = [vp, i32, vp, vp, vp, vp]
+    lib.tdp_cond_blend_records.argtypes = [vp, i32, i32, vp, vp, vp, vp]
     lib.tdp_cond_blend_records.restype = ctypes.c_int
     lib.tdp_tile_mean.argtypes = [vp, ctypes.c_int64, vp, vp, vp]
     lib.tdp_tile_mean.restype = ctypes.c_int
@@ -422,7 +422,7 @@ def tdp_cond_blend_records(plan: Plan, N, recs, Ycond, ncap, out, stream=None):
     B, nt, C, N, ncap = plan.B, plan.n_tiles, plan.C, int(N), int(ncap)
     lat = _latent_dtypes(plan)
     c = _Call("tdp_cond_blend_records")
-    c.run(_lib.tdp_cond_blend_records, plan.handle, N,
+    c.run(_lib.tdp_cond_blend_records, plan.handle, N, ncap,
           c.ptr(recs, "recs", tdp_cond_records_size(plan, N), (torch.int32,), 16),
           c.ptr(Ycond, "Ycond", nt * B * ncap * C, lat, 16), c.ptr(out, "out", B * N * C, lat, 16), stream=stream)
 

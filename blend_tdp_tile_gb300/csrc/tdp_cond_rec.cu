@@ -116,11 +116,11 @@ tdp_cond_record_kernel(const __grid_constant__ tdp_geom g, int32_t N, int32_t nc
 // Block i = the token block whose record is the i-th (tdp_cond_rows.cuh's cond_record_block).
 template <int BF16, int CR>
 __global__ void __launch_bounds__(kTokThreads, kTokMinBlocks)
-tdp_cond_blend_rec_kernel(int32_t nt, int32_t N, int32_t CV, const int32_t *__restrict__ recs,
+tdp_cond_blend_rec_kernel(int32_t nt, int32_t N, uint32_t nrows, int32_t CV, const int32_t *__restrict__ recs,
                           const uint4 *__restrict__ Ycond, uint4 *__restrict__ out)
 {
     extern __shared__ __align__(16) unsigned char dsm[];
-    cond_record_block<BF16, CR>(nt, N, CV, recs, Ycond, out, blockIdx.x, dsm);
+    cond_record_block<BF16, CR>(nt, N, (int32_t)gridDim.x, nrows, CV, recs, Ycond, out, blockIdx.x, dsm);
 }
 
 // Token blocks of a problem and its record layout; TDP_OK when the records apply.
@@ -174,15 +174,18 @@ extern "C" tdp_status tdp_cond_records(tdp_plan_t plan, int32_t N, int32_t ncap,
     return tdp_ok();
 }
 
-extern "C" tdp_status tdp_cond_blend_records(tdp_plan_t plan, int32_t N, const int32_t *recs, const void *Ycond,
-                                             void *out, tdp_stream_t stream)
+extern "C" tdp_status tdp_cond_blend_records(tdp_plan_t plan, int32_t N, int32_t ncap, const int32_t *recs,
+                                             const void *Ycond, void *out, tdp_stream_t stream)
 {
     if (!plan) return tdp_fail(TDP_ERR_INVALID_ARG, "null plan");
     const tdp_geom &g = plan->g;
+    if (ncap < 1) return tdp_fail(TDP_ERR_INVALID_ARG, "need ncap >= 1");
     int64_t G = 0;
     const tdp_status st = rec_shape(g, N, &G);
     if (st != TDP_OK) return st;
     if (G == 0) return tdp_ok();
+    const uint64_t nrows = (uint64_t)g.nt * (uint64_t)g.B * (uint64_t)ncap;
+    if (nrows > 0xffffffffull) return tdp_fail(TDP_ERR_TOO_LARGE, "rows of Ycond numbered past 2^32");
     if (!recs || !Ycond || !out) return tdp_fail(TDP_ERR_INVALID_ARG, "null recs, Ycond or out");
     if (!tdp_aligned(recs, 16) || !tdp_aligned(Ycond, 16) || !tdp_aligned(out, 16))
         return tdp_fail(TDP_ERR_MISALIGNED, "recs, Ycond and out need 16-byte alignment");
@@ -195,16 +198,16 @@ extern "C" tdp_status tdp_cond_blend_records(tdp_plan_t plan, int32_t N, const i
         const size_t smem = rows_layout(g.nt, kRecRows).bytes;
         err = g.dtype == TDP_BF16
                   ? tdp_launch_smem(true, tdp_cond_blend_rec_kernel<1, kRecRows>, (unsigned)G, kTokThreads, smem, s,
-                                    g.nt, N, CV, recs, y, o)
+                                    g.nt, N, (uint32_t)nrows, CV, recs, y, o)
                   : tdp_launch_smem(true, tdp_cond_blend_rec_kernel<0, kRecRows>, (unsigned)G, kTokThreads, smem, s,
-                                    g.nt, N, CV, recs, y, o);
+                                    g.nt, N, (uint32_t)nrows, CV, recs, y, o);
     } else {
         const size_t smem = rows_layout(g.nt).bytes;
         err = g.dtype == TDP_BF16
                   ? tdp_launch_smem(true, tdp_cond_blend_rec_kernel<1, kChunkRows>, (unsigned)G, kTokThreads, smem, s,
-                                    g.nt, N, CV, recs, y, o)
+                                    g.nt, N, (uint32_t)nrows, CV, recs, y, o)
                   : tdp_launch_smem(true, tdp_cond_blend_rec_kernel<0, kChunkRows>, (unsigned)G, kTokThreads, smem, s,
-                                    g.nt, N, CV, recs, y, o);
+                                    g.nt, N, (uint32_t)nrows, CV, recs, y, o);
     }
     if (err == cudaSuccess) err = cudaGetLastError();
     if (err != cudaSuccess) return tdp_fail(TDP_ERR_CUDA, cudaGetErrorString(err));

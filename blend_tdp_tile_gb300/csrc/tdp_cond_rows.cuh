@@ -225,11 +225,11 @@ __device__ __forceinline__ tok_rows rows_from_slots(const tdp_geom &g, int32_t N
 
 // Rows and sums of block b, k0 from its record in shared memory (rec, with the flat list at
 // rec + kRecHead), through a ring of stages of CR rows at dsm: the outputs of its tokens, by
-// the whole block.
+// the whole block.  Rows numbered nrows or more are not read.
 template <int BF16, int CR = kChunkRows>
 __device__ __forceinline__ void rows_sum(int32_t N, int32_t CV, const uint4 *__restrict__ Ycond,
                                          uint4 *__restrict__ out, int32_t b, int32_t k0, const tok_rows &tr,
-                                         unsigned char *dsm, const int32_t *rec)
+                                         unsigned char *dsm, const int32_t *rec, uint32_t nrows = 0xffffffffu)
 {
     uint4 *s_ring = reinterpret_cast<uint4 *>(dsm);
     const uint32_t *s_flat = reinterpret_cast<const uint32_t *>(rec + kRecHead);
@@ -256,7 +256,8 @@ __device__ __forceinline__ void rows_sum(int32_t N, int32_t CV, const uint4 *__r
             for (int i = 0; i < CR * kLanes / kTokThreads; ++i) {
                 const int32_t e = threadIdx.x + i * kTokThreads;
                 const int32_t fi = c * CR + e / kLanes, cv = s * kLanes + e % kLanes;
-                if (fi < R && cv < CV) cp_async16(buf + e, Ycond + (uint64_t)s_flat[fi] * (uint32_t)CV + cv);
+                if (fi < R && cv < CV && s_flat[fi] < nrows)
+                    cp_async16(buf + e, Ycond + (uint64_t)s_flat[fi] * (uint32_t)CV + cv);
             }
         }
         cp_async_commit();
@@ -292,7 +293,9 @@ __device__ __forceinline__ void rows_sum(int32_t N, int32_t CV, const uint4 *__r
 // Record number i of the records tdp_cond_records stores (rec_ints(nt) ints apart from
 // recs) into the record region `rec` of shared memory, by the whole block: its first
 // kFirstInts ints (header and first rows) in one 16-byte load per thread, the rest once R is
-// known; *blk receives its token block.  Ends with a barrier.
+// known; *blk receives its token block.  R and the rows per token are clamped to what a
+// record holds, so that a record not made by tdp_cond_records reads and writes nothing
+// outside its region.  Ends with a barrier.
 constexpr int kFirstInts = 4 * kTokThreads;
 __device__ __forceinline__ tok_rows rows_from_record(int32_t nt, const int32_t *__restrict__ recs, int32_t i,
                                                      int32_t *rec, int32_t *blk)
@@ -305,34 +308,36 @@ __device__ __forceinline__ tok_rows rows_from_record(int32_t nt, const int32_t *
     __syncthreads();
     *blk = rec[0];
     tok_rows tr;
-    tr.R = rec[1];
+    tr.R = min(max(rec[1], 0), kTok * nt);
     for (int32_t e = first + (int32_t)threadIdx.x; e < kRecHead + tr.R; e += kTokThreads) rec[e] = __ldg(src + e);
     const int32_t j = threadIdx.x / kLanes;
-    tr.len = rec[2 + j];
+    tr.len = min(max(rec[2 + j], 0), nt);
     tr.den = rec[2 + kTok + j];
     tr.base = 0;
 #pragma unroll
-    for (int q = 0; q < kTok; ++q) tr.base += q < j ? rec[2 + q] : 0;
+    for (int q = 0; q < kTok; ++q) tr.base += q < j ? min(max(rec[2 + q], 0), nt) : 0;
     __syncthreads();                                      // the whole record is in shared memory
     return tr;
 }
 
 // Block i of the per-call records path: the token block of record i, through a ring of
-// stages of CR rows (rows_layout(nt, CR).bytes of dynamic shared memory at dsm).  Waits for
-// the work before it in the stream before it reads.
+// stages of CR rows (rows_layout(nt, CR).bytes of dynamic shared memory at dsm), G token
+// blocks in all, Ycond rows numbered below nrows.  Waits for the work before it in the
+// stream before it reads.
 template <int BF16, int CR>
-__device__ __forceinline__ void cond_record_block(int32_t nt, int32_t N, int32_t CV, const int32_t *__restrict__ recs,
-                                                  const uint4 *__restrict__ Ycond, uint4 *__restrict__ out, int32_t i,
-                                                  unsigned char *dsm)
+__device__ __forceinline__ void cond_record_block(int32_t nt, int32_t N, int32_t G, uint32_t nrows, int32_t CV,
+                                                  const int32_t *__restrict__ recs, const uint4 *__restrict__ Ycond,
+                                                  uint4 *__restrict__ out, int32_t i, unsigned char *dsm)
 {
     int32_t *rec = reinterpret_cast<int32_t *>(dsm + rows_layout(nt, CR).rec);
     tdp_pdl_trigger();
     tdp_pdl_wait();
     int32_t blk = 0;
     const tok_rows tr = rows_from_record(nt, recs, i, rec, &blk);
+    if (blk < 0 || blk >= G) return;                      // not a record of this problem (block-uniform)
     const int32_t nkb = (N + kTok - 1) / kTok;
     const int32_t b = blk / nkb, k0 = (blk - b * nkb) * kTok;
-    rows_sum<BF16, CR>(N, CV, Ycond, out, b, k0, tr, dsm, rec);
+    rows_sum<BF16, CR>(N, CV, Ycond, out, b, k0, tr, dsm, rec, nrows);
 }
 
 // Block `blk` = tokens k0 .. k0 + kTok - 1 of batch item b (blocks numbered batch item

@@ -296,15 +296,17 @@ tdp_status tdp_cond_blend(tdp_plan_t plan, int32_t N, int32_t ncap, const void *
  *                   row numbers (t*B + b)*ncap + slot of Ycond), then G ints: each token
  *                   block's launch position.
  *   Ycond, out      as for tdp_cond_blend, with the ncap the records were made with.
- * Records made for one plan, N, ncap and slot are valid only for those.  At most 256 tiles
+ * Records made for one plan, N, ncap and slot are valid only for those; a buffer that does
+ * not hold them gives wrong outputs, but tdp_cond_blend_records reads no row of Ycond
+ * numbered n_tiles*B*ncap or more and writes no token outside [B, N).  At most 256 tiles
  * (TDP_ERR_TOO_LARGE beyond; tdp_cond_blend takes any count).  tdp_cond_records runs three
  * kernels; tdp_cond_blend_records one.
  */
 tdp_status tdp_cond_records_size(tdp_plan_t plan, int32_t N, int64_t *ints);
 tdp_status tdp_cond_records(tdp_plan_t plan, int32_t N, int32_t ncap, const int32_t *slot, int32_t *recs,
                             tdp_stream_t stream);
-tdp_status tdp_cond_blend_records(tdp_plan_t plan, int32_t N, const int32_t *recs, const void *Ycond, void *out,
-                                  tdp_stream_t stream);
+tdp_status tdp_cond_blend_records(tdp_plan_t plan, int32_t N, int32_t ncap, const int32_t *recs, const void *Ycond,
+                                  void *out, tdp_stream_t stream);
 
 /*
  * tdp_blend_cond -- the post-model stage in one call: tdp_blend and tdp_cond_blend with

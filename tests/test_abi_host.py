@@ -232,7 +232,7 @@ def test_cond_records_size_and_refusals(tdp):
     vp, i32 = ctypes.c_void_p, ctypes.c_int32
     lib.tdp_cond_records_size.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_int64)]
     lib.tdp_cond_records.argtypes = [vp, i32, i32, vp, vp, vp]
-    lib.tdp_cond_blend_records.argtypes = [vp, i32, vp, vp, vp, vp]
+    lib.tdp_cond_blend_records.argtypes = [vp, i32, i32, vp, vp, vp, vp]
     for wl in wk.WORKLOADS:
         plan = tdp.tdp_plan_create(wl.B, wl.F, wl.H, wl.W, wl.C, wl.dtype, wl.num_tiles, wl.overlap)
         G = wl.B * ((wl.n_cond + 7) // 8)
@@ -245,7 +245,8 @@ def test_cond_records_size_and_refusals(tdp):
     assert lib.tdp_cond_records_size(None, 4, ctypes.byref(n)) == 1
     # N = 0: nothing to do, nothing read
     assert lib.tdp_cond_records(plan.handle, 0, 1, None, None, None) == 0
-    assert lib.tdp_cond_blend_records(plan.handle, 0, None, None, None, None) == 0
+    assert lib.tdp_cond_blend_records(plan.handle, 0, 1, None, None, None, None) == 0
+    assert lib.tdp_cond_blend_records(plan.handle, 4, 0, None, None, None, None) == 1      # ncap < 1
     assert lib.tdp_cond_records(plan.handle, 4, 0, None, None, None) == 1          # ncap < 1
     assert lib.tdp_cond_records(plan.handle, 4, 1, None, None, None) == 1          # null slot
     # 257 tiles or more: beyond the records (tdp_cond_blend takes them)
@@ -253,7 +254,7 @@ def test_cond_records_size_and_refusals(tdp):
     assert big.n_tiles > 256
     assert lib.tdp_cond_records_size(big.handle, 8, ctypes.byref(n)) == 5
     assert lib.tdp_cond_records(big.handle, 8, 1, None, None, None) == 5
-    assert lib.tdp_cond_blend_records(big.handle, 8, None, None, None, None) == 5
+    assert lib.tdp_cond_blend_records(big.handle, 8, 1, None, None, None, None) == 5
 
 
 @no_gpu_only
@@ -261,10 +262,10 @@ def test_cond_records_alignment_refused_on_host(tdp):
     lib = ctypes.CDLL(tdp.LIB_PATH)
     vp, i32 = ctypes.c_void_p, ctypes.c_int32
     lib.tdp_cond_records.argtypes = [vp, i32, i32, vp, vp, vp]
-    lib.tdp_cond_blend_records.argtypes = [vp, i32, vp, vp, vp, vp]
+    lib.tdp_cond_blend_records.argtypes = [vp, i32, i32, vp, vp, vp, vp]
     plan = tdp.tdp_plan_create(1, 3, 8, 12, 16, "f32", (1, 2, 2), (0, 2, 2))
     assert lib.tdp_cond_records(plan.handle, 4, 1, 16, 8, None) == 4               # recs not 16-byte aligned
     assert lib.tdp_cond_records(plan.handle, 4, 1, 6, 16, None) == 4               # slot not 4-byte aligned
-    assert lib.tdp_cond_blend_records(plan.handle, 4, 8, 16, 16, None) == 4
-    assert lib.tdp_cond_blend_records(plan.handle, 4, 16, 24, 16, None) == 4
-    assert lib.tdp_cond_blend_records(plan.handle, 4, 16, 16, None, None) == 1
+    assert lib.tdp_cond_blend_records(plan.handle, 4, 1, 8, 16, 16, None) == 4
+    assert lib.tdp_cond_blend_records(plan.handle, 4, 1, 16, 24, 16, None) == 4
+    assert lib.tdp_cond_blend_records(plan.handle, 4, 1, 16, 16, None, None) == 1

@@ -157,3 +157,30 @@ def test_records_at_the_tile_limit(tdp):
     for _, O1, O2 in res:
         assert _same(O1, O2)
 
+
+
+def test_foreign_records_stay_in_bounds(tdp):
+    """A buffer that does not hold records (random integers, huge row counts and row numbers):
+    the outputs are meaningless, but nothing outside Ycond is read and nothing outside out is
+    written (guard bands around out keep their bytes)."""
+    import torch
+    wl = wk.by_name("small")
+    plan, out, N, ncap = _setup(tdp, wl)
+    g = torch.Generator(device="cuda").manual_seed(5)
+    n = tdp.tdp_cond_records_size(plan, N)
+    recs = torch.randint(-2**31, 2**31 - 1, (n,), generator=g, device="cuda", dtype=torch.int64).to(torch.int32)
+    Yc = to_dev(_storage(wl, (plan.n_tiles, wl.B, ncap, wl.C), 3))
+    pad = 4096
+    big = fill_sentinel(torch.empty(wl.B * N * wl.C + 2 * pad, dtype=torch.bfloat16, device="cuda"))
+    ref = big.clone()
+    tdp.tdp_cond_blend_records(plan, N, recs, Yc, ncap, big[pad:pad + wl.B * N * wl.C])
+    torch.cuda.synchronize()
+    assert _same(big[:pad], ref[:pad]) and _same(big[-pad:], ref[-pad:])
+    # the same buffer with plausible block numbers: every record's block in [0, G)
+    G = wl.B * ((N + TOK - 1) // TOK)
+    stride = (HEAD + TOK * plan.n_tiles + 3) // 4 * 4
+    r = recs[:G * stride].view(G, stride)
+    r[:, 0] = torch.arange(G, device="cuda", dtype=torch.int32)
+    tdp.tdp_cond_blend_records(plan, N, recs, Yc, ncap, big[pad:pad + wl.B * N * wl.C])
+    torch.cuda.synchronize()
+    assert _same(big[:pad], ref[:pad]) and _same(big[-pad:], ref[-pad:])
