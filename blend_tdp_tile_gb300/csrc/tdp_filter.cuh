@@ -18,7 +18,6 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kSub = 16;                          // tokens per thread and chunk
 constexpr int kChunk = kThreads * kSub;           // tokens per chunk
 constexpr int kCountTok = 64;                     // tokens per keep-count block
-constexpr int kCountGroups = kThreads / kCountTok;
 constexpr int kTileStage = 1024;                  // tile bounds staged in shared memory at once
 
 __device__ __forceinline__ bool keeps(const int2 (&k)[3], const int32_t (&lo)[3], const int32_t (&hi)[3])
@@ -40,16 +39,21 @@ __device__ __forceinline__ void load_bounds(const int32_t *mn, const int32_t *mx
 }
 
 // ---- kcount[b, k] for the kCountTok tokens of block `blk` (blocks are (b, token
-// range) in b-major order): thread (group, token) tests tiles t = group mod
-// kCountGroups against bounds staged in shared memory; the groups' counts are summed.
-struct kcount_smem {
+// range) in b-major order), by a block of T threads: thread (group, token) tests tiles
+// t = group mod T / kCountTok against bounds staged in shared memory; the groups' counts
+// are summed.
+template <int T>
+struct kcount_smem_t {
     int32_t lo[kTileStage][3], hi[kTileStage][3];
-    int32_t cnt[kCountGroups][kCountTok];
+    int32_t cnt[T / kCountTok][kCountTok];
 };
+using kcount_smem = kcount_smem_t<kThreads>;
 
+template <int T = kThreads>
 __device__ __forceinline__ void kcount_block(const tdp_geom &g, const int2 *K, int32_t N, const int32_t *mn,
-                                             const int32_t *mx, int32_t *kcount, int32_t blk, kcount_smem &sm)
+                                             const int32_t *mx, int32_t *kcount, int32_t blk, kcount_smem_t<T> &sm)
 {
+    constexpr int kCountGroups = T / kCountTok;
     const int32_t nkb = (N + kCountTok - 1) / kCountTok;
     const int32_t b = blk / nkb;
     const int32_t tok = threadIdx.x % kCountTok, grp = threadIdx.x / kCountTok;
@@ -87,19 +91,22 @@ __device__ __forceinline__ void kcount_block(const tdp_geom &g, const int2 *K, i
     }
 }
 
-// ---- compaction of one chunk of kChunk tokens.  Thread (warp w, lane l) owns
-// tokens k0 + j*kThreads + w*32 + l, j < kSub; ballots[j] are its warp's keep
-// ballots.  Positions follow (j, w, l) order, i.e. ascending k.
-struct compact_smem {
-    int32_t off[kSub][kWarps];
-    int32_t sum[kWarps][2];
+// ---- compaction of one chunk of T * kSub tokens by a block of T threads.  Thread
+// (warp w, lane l) owns tokens k0 + j*T + w*32 + l, j < kSub; ballots[j] are its warp's
+// keep ballots.  Positions follow (j, w, l) order, i.e. ascending k.
+template <int T>
+struct compact_smem_t {
+    int32_t off[kSub][T / 32];
     int32_t total;
 };
+using compact_smem = compact_smem_t<kThreads>;
 
 // sm.off[j][w] = base + kept tokens of the chunk before sub-chunk j of warp w;
 // returns the chunk's kept count.  Every thread calls it; ends with a barrier.
-__device__ __forceinline__ int32_t chunk_offsets(const uint32_t (&ballots)[kSub], int32_t base, compact_smem &sm)
+template <int T = kThreads>
+__device__ __forceinline__ int32_t chunk_offsets(const uint32_t (&ballots)[kSub], int32_t base, compact_smem_t<T> &sm)
 {
+    constexpr int kWarps = T / 32;
     const int32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (lane < kSub) {
         uint32_t mine = 0;
@@ -140,15 +147,16 @@ __device__ __forceinline__ int32_t chunk_offsets(const uint32_t (&ballots)[kSub]
 }
 
 // Write slot / idx / Kout for one chunk whose offsets chunk_offsets() filled.
+template <int T = kThreads>
 __device__ __forceinline__ void chunk_write(const int2 *Kb, int32_t N, int64_t tb, int32_t k0,
                                             const uint32_t (&ballots)[kSub], const int32_t (&shift)[3],
-                                            const compact_smem &sm, int32_t *idx, int2 *Kout, int32_t *slot)
+                                            const compact_smem_t<T> &sm, int32_t *idx, int2 *Kout, int32_t *slot)
 {
     const int32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t lt_mask = (1u << lane) - 1u;
 #pragma unroll
     for (int j = 0; j < kSub; ++j) {
-        const int32_t k = k0 + j * kThreads + threadIdx.x;
+        const int32_t k = k0 + j * T + threadIdx.x;
         const bool kept = (ballots[j] >> lane) & 1u;
         const int32_t pos = sm.off[j][warp] + __popc(ballots[j] & lt_mask);
         if (slot && k < N) slot[tb * N + k] = kept ? pos : -1;
@@ -165,13 +173,14 @@ __device__ __forceinline__ void chunk_write(const int2 *Kb, int32_t N, int64_t t
     }
 }
 
-// ---- the whole filter of one (tile, batch item) row tb = t*B + b in one
-// block: keep test, keep bytes, stable compaction chunk by chunk with a
-// running base, -1 padding of idx and the count.
+// ---- the whole filter of one (tile, batch item) row tb = t*B + b in one block of T
+// threads: keep test, keep bytes, stable compaction chunk by chunk (T * kSub tokens
+// each) with a running base, -1 padding of idx and the count.
+template <int T = kThreads>
 __device__ __forceinline__ void tb_block(const tdp_geom &g, const int2 *K, int32_t N, const int32_t *mn,
                                          const int32_t *mx, int32_t normalize, int64_t tb, uint8_t *keep,
                                          int32_t *idx, int32_t *count, int2 *Kout, int32_t *slot,
-                                         compact_smem &sm)
+                                         compact_smem_t<T> &sm)
 {
     const int32_t b = (int32_t)(tb % g.B);
     const int2 *Kb = K + (int64_t)b * 3 * N;
@@ -179,11 +188,11 @@ __device__ __forceinline__ void tb_block(const tdp_geom &g, const int2 *K, int32
     load_bounds(mn, mx, tb, lo, hi);
     const int32_t shift[3] = {normalize ? lo[0] : 0, normalize ? lo[1] : 0, normalize ? lo[2] : 0};
     int32_t run = 0;
-    for (int32_t k0 = 0; k0 < N; k0 += kChunk) {
+    for (int32_t k0 = 0; k0 < N; k0 += T * kSub) {
         uint32_t ballots[kSub];
 #pragma unroll
         for (int j = 0; j < kSub; ++j) {
-            const int32_t k = k0 + j * kThreads + threadIdx.x;
+            const int32_t k = k0 + j * T + threadIdx.x;
             bool kept = false;
             if (k < N) {
                 const int2 kv[3] = {__ldg(Kb + k), __ldg(Kb + (int64_t)N + k), __ldg(Kb + 2 * (int64_t)N + k)};
@@ -192,8 +201,8 @@ __device__ __forceinline__ void tb_block(const tdp_geom &g, const int2 *K, int32
             }
             ballots[j] = __ballot_sync(0xffffffffu, kept);
         }
-        const int32_t tot = chunk_offsets(ballots, run, sm);
-        chunk_write(Kb, N, tb, k0, ballots, shift, sm, idx, Kout, slot);
+        const int32_t tot = chunk_offsets<T>(ballots, run, sm);
+        chunk_write<T>(Kb, N, tb, k0, ballots, shift, sm, idx, Kout, slot);
         run += tot;
         __syncthreads();                      // the next chunk rewrites sm.off / sm.total
     }

@@ -2,10 +2,16 @@
 // ("Tiled Data Parallelism (TDP)", sections "Shared negative (reference)
 // positions" and "Position normalization").
 //
-// Two launches, both over (tile, batch item, chunk of 4096 tokens) blocks so
-// that the work spreads over the whole GPU even with few tiles; no scratch
-// memory (the keep output carries what the second launch needs), no atomics,
-// no block waits on another:
+// No scratch memory, no atomics, no block waits on another.  Two forms:
+//
+// Up to kOneChunk tokens (one chunk per (tile, batch item)): one launch,
+// tdp_filter_kernel, of two kinds of 512-thread block: a filter block per (tile, batch
+// item), tdp_filter.cuh's tb_block (keep test, keep bytes, stable compaction, -1 padding,
+// count), and count blocks (the tiles that keep each token).
+//
+// More tokens: two launches, both over (tile, batch item, chunk of 4096 tokens) blocks so
+// that the work spreads over the whole GPU even with few tiles (the keep output carries
+// what the second launch needs):
 //   1. tdp_keep_kernel: every thread tests 16 tokens of its chunk, 256 apart
 //      (coalesced), against the tile's position extent [mn, mx) and writes the
 //      keep byte.  Extra blocks count, for each token, the tiles that keep it
@@ -23,6 +29,28 @@
 namespace {
 
 using namespace tdp_filt;
+
+constexpr int kOneThreads = 512;                      // threads of the one-launch form's blocks
+constexpr int kOneChunk = kOneThreads * kSub;         // most tokens the one-launch form takes
+
+// Blocks [0, nfilt): filter blocks (tb = t*B + b); [nfilt, nfilt + ncount): count blocks.
+__global__ void __launch_bounds__(kOneThreads)
+tdp_filter_kernel(const __grid_constant__ tdp_geom g, const int2 *__restrict__ K, int32_t N,
+                  const int32_t *__restrict__ mn, const int32_t *__restrict__ mx, int32_t normalize,
+                  uint8_t *__restrict__ keep, int32_t *__restrict__ idx, int32_t *__restrict__ count,
+                  int32_t *__restrict__ kcount, int2 *__restrict__ Kout, int32_t *__restrict__ slot, int32_t nfilt)
+{
+    __shared__ union {
+        compact_smem_t<kOneThreads> compact;
+        kcount_smem_t<kOneThreads> kc;
+    } sm;
+    // No early trigger: the next kernel launches as these latency-bound blocks exit.
+    tdp_pdl_wait();
+    if ((int32_t)blockIdx.x < nfilt)
+        tb_block<kOneThreads>(g, K, N, mn, mx, normalize, blockIdx.x, keep, idx, count, Kout, slot, sm.compact);
+    else
+        kcount_block<kOneThreads>(g, K, N, mn, mx, kcount, (int32_t)blockIdx.x - nfilt, sm.kc);
+}
 
 __global__ void __launch_bounds__(kThreads)
 tdp_keep_kernel(const __grid_constant__ tdp_geom g, const int2 *__restrict__ K, int32_t N, int32_t nchunk,
@@ -84,6 +112,7 @@ tdp_compact_kernel(const __grid_constant__ tdp_geom g, const int2 *__restrict__ 
                    int2 *__restrict__ Kout, int32_t *__restrict__ slot)
 {
     __shared__ compact_smem sm;
+    __shared__ int32_t s_sum[kWarps][2];
     tdp_pdl_wait();
     const int64_t tb = blockIdx.x / nchunk;
     const int32_t c = (int32_t)(blockIdx.x - tb * nchunk);
@@ -108,7 +137,7 @@ tdp_compact_kernel(const __grid_constant__ tdp_geom g, const int2 *__restrict__ 
             before += i < k0 ? n : 0;
         }
     }
-    block_sum2(before, total, sm.sum);
+    block_sum2(before, total, s_sum);
 
     // ---- this chunk: ballots per (sub-chunk, warp), offsets from one scan
     uint32_t ballots[kSub];
@@ -156,6 +185,15 @@ extern "C" tdp_status tdp_norm_filter(tdp_plan_t plan, const int32_t *K, int32_t
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int2 *k2 = reinterpret_cast<const int2 *>(K);
     cudaError_t err = cudaSuccess;
+    if (N <= kOneChunk) {
+        const int64_t ncount = (int64_t)g.B * ((N + kCountTok - 1) / kCountTok);
+        err = tdp_launch(true, tdp_filter_kernel, (unsigned)(g.nt * (int64_t)g.B + ncount), kOneThreads, s, g, k2, N,
+                         mn, mx, normalize, keep, idx, count, kcount, reinterpret_cast<int2 *>(Kout), slot,
+                         (int32_t)(g.nt * (int64_t)g.B));
+        if (err == cudaSuccess) err = cudaGetLastError();
+        if (err != cudaSuccess) return tdp_fail(TDP_ERR_CUDA, cudaGetErrorString(err));
+        return tdp_ok();
+    }
     if (N > 0)
         err = tdp_launch(true, tdp_keep_kernel, (unsigned)blocks1, kThreads, s, g, k2, N, nchunk, mn, mx, keep,
                          kcount);
