@@ -945,6 +945,10 @@ def main():
             dist.destroy_process_group()
     finally:
         sys.stdout.flush()
+        # C stdio buffers (NCCL writes its banner through them) are flushed here, while
+        # fd 1 still points at stderr, not at exit after the JSON line
+        import ctypes
+        ctypes.CDLL(None).fflush(None)
         os.dup2(saved, 1)
         os.close(saved)
     if rank == 0:
