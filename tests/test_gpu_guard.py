@@ -9,7 +9,8 @@ guard band of GUARD bytes on each side:
   element-by-element comparison with the CPU oracle would fail.
 
 Each case runs every entry point: tdp_pos_bounds, tdp_split, tdp_split_tma,
-tdp_norm_filter, tdp_split_filter, tdp_blend, tdp_cond_blend, tdp_blend_cond and
+tdp_norm_filter, tdp_split_filter, tdp_blend, tdp_cond_blend, tdp_cond_records and
+tdp_cond_blend_records (where the tiles are 256 or fewer), tdp_blend_cond and
 tdp_tile_mean, on ragged
 geometries (tails in every dimension, several batch items, minimal and odd
 channel counts).  Method: "Tiled Data Parallelism (TDP)" (LTX-2 docs, multigpu).
@@ -171,6 +172,16 @@ def test_guard_bands(tdp, name, wl):
     torch.cuda.synchronize()
     _check_bands({"out": Rg}, "tdp_cond_blend")
     assert_blend_close(_host(Rg), oracle.cond_blend(p, Yc, ref["keep"], ref["idx"], ref["count"], ncap), wl)
+
+    # the same outputs from per-block records (the records take at most 256 tiles)
+    if nt <= 256:
+        Rec = _output((tdp.tdp_cond_records_size(plan, N),), i32)
+        tdp.tdp_cond_records(plan, N, ncap, Sg.t, Rec.t)
+        Rg3 = _output((B, N, C), lat)
+        tdp.tdp_cond_blend_records(plan, N, Rec.t, Ycg.t, ncap, Rg3.t)
+        torch.cuda.synchronize()
+        _check_bands({"recs": Rec, "out": Rg3}, "tdp_cond_records / tdp_cond_blend_records")
+        assert np.array_equal(_host(Rg3), _host(Rg)), "tdp_cond_blend_records"
 
     # the post-model stage in one call: the same bytes as the two calls above
     Zg2, Rg2 = _output((B, wl.F, wl.H, wl.W, C), lat), _output((B, N, C), lat)
