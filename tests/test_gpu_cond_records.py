@@ -108,6 +108,16 @@ def test_records_match_the_slot_path(tdp, name):
         _check_records(plan, wl, out, N, ncap, recs)
 
 
+def test_records_with_half_the_tokens_kept_by_every_tile(tdp):
+    """The large workload with half its tokens at negative time (kept by all 128 tiles): blocks
+    of up to 1024 rows, many ring stages each."""
+    wl = wk.by_name("large").replace(neg_frac=0.5)
+    plan, out, N, ncap = _setup(tdp, wl)
+    recs, res = _blends(tdp, plan, wl, out, N, ncap)
+    for _, O1, O2 in res:
+        assert _same(O1, O2)
+
+
 @pytest.mark.parametrize("ncap", [1, 7])
 def test_records_with_rows_past_capacity(tdp, ncap):
     wl = wk.by_name("small").replace(B=2, n_cond=1003)
