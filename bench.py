@@ -693,7 +693,7 @@ def run_ours(args, rank, world, local_rank):
             flush = L2Flush(torch, dev)
             rec_ms = call_ms(torch, s, lambda: tdp.tdp_cond_records(plan, N, ncap, slot2, recs, stream=s), 10, flush)
             nblk = wl.B * ((N + 7) // 8)
-            rec_bytes = (kept_rows * wl.C * wl.esize + nblk * 18 * 4 + kept_rows * 4 + wl.B * N * wl.C * wl.esize)
+            rec_bytes = (kept_rows * wl.C * wl.esize + nblk * 26 * 4 + kept_rows * 4 + wl.B * N * wl.C * wl.esize)
             extras["cond_blend_records"] = call_entry(
                 call_ms(torch, s, lambda: tdp.tdp_cond_blend_records(plan, N, recs, Yc, ncap, Oc, stream=s), reps,
                         flush), rec_bytes, peak)

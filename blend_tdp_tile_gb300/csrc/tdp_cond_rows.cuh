@@ -86,14 +86,15 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-// A token block's record: what the rows and sums of its tokens need, in int32 units
+// A block's record: what the rows and sums of its kTok tokens need, in int32 units
 //   [0] block number   [1] R, its stored rows   [2, 2 + kTok) rows per token (len)
 //   [2 + kTok, 2 + 2 kTok) tiles that kept each token (den)
+//   [2 + 2 kTok, 2 + 3 kTok) each token's index b N + k (its output row), -1 for none
 //   [kRecHead, kRecHead + R) the rows of Ycond, token after token, each token's in
 //   ascending tile order (the flat list).
 // It lives in shared memory while a block works, and tdp_cond_records stores one per block
 // in global memory, rec_ints(nt) apart.
-constexpr int kRecHead = 2 + 2 * kTok;
+constexpr int kRecHead = 2 + 3 * kTok;
 __host__ __device__ constexpr int64_t rec_ints(int32_t nt)
 {
     return ((int64_t)kRecHead + (int64_t)kTok * nt + 3) & ~(int64_t)3;
@@ -116,23 +117,35 @@ static_assert((((size_t)kStageTiles * (kTok + 1) * 4 + 15) & ~(size_t)15) + (siz
                   (size_t)kStages * kChunkRows * kLanes * 16,
               "the staged slots and the per-token lists fit in the row ring");
 
-// s_slot[t][j] (row stride kTok + 1) = slot of token k0 + j in tile t, for tiles up to
-// MAXT >= nt (-1 for tokens past N), by the whole block: thread (j, t0) loads tiles t0,
-// t0 + kTokThreads / kTok, ..., each warp load covering 4 tiles x 8 tokens (4 whole
-// 32-byte sectors), all its loads in flight before any is stored.
-template <int MAXT>
-__device__ __forceinline__ void stage_slots(const int32_t *__restrict__ slot, int32_t nt, int32_t B, int32_t N,
-                                            int32_t b, int32_t k0, int32_t *s_slot)
+// The tokens a block works on.  A token is its index b N + k, which is also its offset in a
+// tile's slots (slot[t][b][k] = slot[t B N + b N + k]); -1 is no token.
+struct block_tokens {        // tokens k0 .. k0 + kTok - 1 of batch item b (the slot path)
+    int64_t base;            // b N + k0
+    int32_t left;            // N - k0
+    __device__ __forceinline__ int64_t tok(int32_t j) const { return j < left ? base + j : -1; }
+};
+struct dealt_tokens {        // tokens dealt to a record, in shared memory
+    const int32_t *s;
+    __device__ __forceinline__ int64_t tok(int32_t j) const { return s[j]; }
+};
+
+// s_slot[t][j] (row stride kTok + 1) = slot of token ts.tok(j) in tile t, for tiles up to
+// MAXT >= nt (-1 for no token), by the whole block: thread (j, t0) loads tiles t0,
+// t0 + kTokThreads / kTok, ..., all its loads in flight before any is stored (for
+// consecutive tokens each warp load covers 4 tiles x 8 tokens, 4 whole 32-byte sectors).
+template <int MAXT, class TS>
+__device__ __forceinline__ void stage_slots(const int32_t *__restrict__ slot, int32_t nt, int64_t BN, const TS &ts,
+                                            int32_t *s_slot)
 {
     constexpr int kStep = kTokThreads / kTok;      // tiles per pass of the block
     constexpr int kPer = MAXT / kStep;             // loads per thread
     const int32_t j = threadIdx.x % kTok, t0 = threadIdx.x / kTok;
-    const bool tok_ok = k0 + j < N;
+    const int64_t tk = ts.tok(j);
     int32_t v[kPer];
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
         const int32_t t = t0 + u * kStep;
-        v[u] = t < nt && tok_ok ? __ldg(slot + ((int64_t)t * B + b) * N + k0 + j) : -1;
+        v[u] = t < nt && tk >= 0 ? __ldg(slot + (int64_t)t * BN + tk) : -1;
     }
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
@@ -175,23 +188,27 @@ struct tok_rows {
     int32_t len, den, base, R;
 };
 
-// The record of block blk (tokens k0 .. k0 + kTok - 1 of batch item b) from the slots, into
-// the record region `rec` of shared memory, by the whole block; ends with a barrier.
+// The record of block blk (tokens ts.tok(0 .. kTok - 1)) from the slots, into the record
+// region `rec` of shared memory, by the whole block; ends with a barrier.
+template <class TS>
 __device__ __forceinline__ tok_rows rows_from_slots(const tdp_geom &g, int32_t N, int32_t ncap,
-                                                    const int32_t *__restrict__ slot, int32_t blk, int32_t b,
-                                                    int32_t k0, unsigned char *dsm, int32_t *rec)
+                                                    const int32_t *__restrict__ slot, int32_t blk, const TS &ts,
+                                                    unsigned char *dsm, int32_t *rec)
 {
     const int32_t nt = g.nt;
+    const int64_t BN = (int64_t)g.B * N;
     int32_t *s_slot = reinterpret_cast<int32_t *>(dsm);
     // 1. slots
     if (nt <= kStageTiles / 2)
-        stage_slots<kStageTiles / 2>(slot, nt, g.B, N, b, k0, s_slot);
+        stage_slots<kStageTiles / 2>(slot, nt, BN, ts, s_slot);
     else
-        stage_slots<kStageTiles>(slot, nt, g.B, N, b, k0, s_slot);
+        stage_slots<kStageTiles>(slot, nt, BN, ts, s_slot);
     __syncthreads();
-    // 2. lists: half-warp j, token k = k0 + j; lane h looks at tiles u*16 + h, so the
-    // token's stored rows come out in ascending tile order (u, then h)
+    // 2. lists: half-warp j, token ts.tok(j) of batch item b; lane h looks at tiles u*16 + h,
+    // so the token's stored rows come out in ascending tile order (u, then h)
     const int32_t j = threadIdx.x / kLanes, h = threadIdx.x % kLanes;
+    const int64_t tk = ts.tok(j);
+    const int32_t b = tk >= 0 ? (int32_t)(tk / N) : 0;
     uint32_t *s_row = reinterpret_cast<uint32_t *>(dsm + (((size_t)nt * (kTok + 1) * 4 + 15) & ~(size_t)15)) + j * nt;
     tok_rows tr;
     tr.len = 0;
@@ -203,6 +220,7 @@ __device__ __forceinline__ tok_rows rows_from_slots(const tdp_geom &g, int32_t N
     if (h == 0) {
         rec[2 + j] = tr.len;
         rec[2 + kTok + j] = tr.den;
+        rec[2 + 2 * kTok + j] = (int32_t)tk;
     }
     __syncthreads();
     tr.base = 0;
@@ -223,25 +241,25 @@ __device__ __forceinline__ tok_rows rows_from_slots(const tdp_geom &g, int32_t N
     return tr;
 }
 
-// Rows and sums of block b, k0 from its record in shared memory (rec, with the flat list at
+// Rows and sums of a block from its record in shared memory (rec, with the flat list at
 // rec + kRecHead), through a ring of stages of CR rows at dsm: the outputs of its tokens, by
-// the whole block.  Rows numbered nrows or more are not read.
+// the whole block; this thread's token writes output row otok (none when otok < 0).  Rows
+// numbered nrows or more are not read.
 template <int BF16, int CR = kChunkRows>
-__device__ __forceinline__ void rows_sum(int32_t N, int32_t CV, const uint4 *__restrict__ Ycond,
-                                         uint4 *__restrict__ out, int32_t b, int32_t k0, const tok_rows &tr,
-                                         unsigned char *dsm, const int32_t *rec, uint32_t nrows = 0xffffffffu)
+__device__ __forceinline__ void rows_sum(int32_t CV, const uint4 *__restrict__ Ycond, uint4 *__restrict__ out,
+                                         int64_t otok, const tok_rows &tr, unsigned char *dsm, const int32_t *rec,
+                                         uint32_t nrows = 0xffffffffu)
 {
     uint4 *s_ring = reinterpret_cast<uint4 *>(dsm);
     const uint32_t *s_flat = reinterpret_cast<const uint32_t *>(rec + kRecHead);
     const int32_t h = threadIdx.x % kLanes;
-    const int32_t k = k0 + (int32_t)threadIdx.x / kLanes;
     const int32_t R = tr.R, base = tr.base, len = tr.len;
     static_assert((CR * kLanes) % kTokThreads == 0, "the copies of a stage split evenly over the block");
     const int32_t nslab = (CV + kLanes - 1) / kLanes;
-    const bool tok_ok = k < N;
+    const bool tok_ok = otok >= 0;
     if (R == 0) {      // no stored row in the block: every output is 0
         for (int32_t cv = h; cv < CV; cv += kLanes)
-            if (tok_ok) __stcs(out + ((int64_t)b * N + k) * CV + cv, make_uint4(0u, 0u, 0u, 0u));
+            if (tok_ok) __stcs(out + otok * CV + cv, make_uint4(0u, 0u, 0u, 0u));
         return;
     }
     // 3. rows: units q = (slab of kLanes channel vectors, chunk of CR rows of the
@@ -280,7 +298,7 @@ __device__ __forceinline__ void rows_sum(int32_t N, int32_t CV, const uint4 *__r
         }
         if (c == nch - 1) {                                   // the slab's last chunk: the output
             if (tok_ok && cv < CV)
-                __stcs(out + ((int64_t)b * N + k) * CV + cv,
+                __stcs(out + otok * CV + cv,
                        tr.den > 0 ? acc_weigh<BF16>(acc, (float)tr.den) : make_uint4(0u, 0u, 0u, 0u));
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[e] = 0.f;
@@ -293,12 +311,13 @@ __device__ __forceinline__ void rows_sum(int32_t N, int32_t CV, const uint4 *__r
 // Record number i of the records tdp_cond_records stores (rec_ints(nt) ints apart from
 // recs) into the record region `rec` of shared memory, by the whole block: its first
 // kFirstInts ints (header and first rows) in one 16-byte load per thread, the rest once R is
-// known; *blk receives its token block.  R and the rows per token are clamped to what a
-// record holds, so that a record not made by tdp_cond_records reads and writes nothing
-// outside its region.  Ends with a barrier.
+// known; *blk receives its block number and *otok this thread's output token (-1 unless in
+// [0, ntok)).  R and the rows per token are clamped to what a record holds, so that a record
+// not made by tdp_cond_records reads and writes nothing outside its region and out.  Ends
+// with a barrier.
 constexpr int kFirstInts = 4 * kTokThreads;
-__device__ __forceinline__ tok_rows rows_from_record(int32_t nt, const int32_t *__restrict__ recs, int32_t i,
-                                                     int32_t *rec, int32_t *blk)
+__device__ __forceinline__ tok_rows rows_from_record(int32_t nt, int64_t ntok, const int32_t *__restrict__ recs,
+                                                     int32_t i, int32_t *rec, int32_t *blk, int64_t *otok)
 {
     const int64_t stride = rec_ints(nt);
     const int32_t *src = recs + (int64_t)i * stride;
@@ -313,6 +332,8 @@ __device__ __forceinline__ tok_rows rows_from_record(int32_t nt, const int32_t *
     const int32_t j = threadIdx.x / kLanes;
     tr.len = min(max(rec[2 + j], 0), nt);
     tr.den = rec[2 + kTok + j];
+    const int32_t ot = rec[2 + 2 * kTok + j];
+    *otok = ot >= 0 && ot < ntok ? ot : -1;
     tr.base = 0;
 #pragma unroll
     for (int q = 0; q < kTok; ++q) tr.base += q < j ? min(max(rec[2 + q], 0), nt) : 0;
@@ -320,12 +341,12 @@ __device__ __forceinline__ tok_rows rows_from_record(int32_t nt, const int32_t *
     return tr;
 }
 
-// Block i of the per-call records path: the token block of record i, through a ring of
-// stages of CR rows (rows_layout(nt, CR).bytes of dynamic shared memory at dsm), G token
-// blocks in all, Ycond rows numbered below nrows.  Waits for the work before it in the
-// stream before it reads.
+// Block i of the per-call records path: the tokens of record i, through a ring of stages
+// of CR rows (rows_layout(nt, CR).bytes of dynamic shared memory at dsm), G records and ntok
+// tokens (output rows) in all, Ycond rows numbered below nrows.  Waits for the work before
+// it in the stream before it reads.
 template <int BF16, int CR>
-__device__ __forceinline__ void cond_record_block(int32_t nt, int32_t N, int32_t G, uint32_t nrows, int32_t CV,
+__device__ __forceinline__ void cond_record_block(int32_t nt, int64_t ntok, int32_t G, uint32_t nrows, int32_t CV,
                                                   const int32_t *__restrict__ recs, const uint4 *__restrict__ Ycond,
                                                   uint4 *__restrict__ out, int32_t i, unsigned char *dsm)
 {
@@ -333,11 +354,10 @@ __device__ __forceinline__ void cond_record_block(int32_t nt, int32_t N, int32_t
     tdp_pdl_trigger();
     tdp_pdl_wait();
     int32_t blk = 0;
-    const tok_rows tr = rows_from_record(nt, recs, i, rec, &blk);
+    int64_t otok = -1;
+    const tok_rows tr = rows_from_record(nt, ntok, recs, i, rec, &blk, &otok);
     if (blk < 0 || blk >= G) return;                      // not a record of this problem (block-uniform)
-    const int32_t nkb = (N + kTok - 1) / kTok;
-    const int32_t b = blk / nkb, k0 = (blk - b * nkb) * kTok;
-    rows_sum<BF16, CR>(N, CV, Ycond, out, b, k0, tr, dsm, rec, nrows);
+    rows_sum<BF16, CR>(CV, Ycond, out, otok, tr, dsm, rec, nrows);
 }
 
 // Block `blk` = tokens k0 .. k0 + kTok - 1 of batch item b (blocks numbered batch item
@@ -354,8 +374,9 @@ __device__ __forceinline__ void cond_rows_block(const tdp_geom &g, int32_t N, in
     tdp_pdl_wait();
     const int32_t nkb = (N + kTok - 1) / kTok;
     const int32_t b = blk / nkb, k0 = (blk - b * nkb) * kTok;
-    const tok_rows tr = rows_from_slots(g, N, ncap, slot, blk, b, k0, dsm, rec);
-    rows_sum<BF16>(N, CV, Ycond, out, b, k0, tr, dsm, rec);
+    const block_tokens ts{(int64_t)b * N + k0, N - k0};
+    const tok_rows tr = rows_from_slots(g, N, ncap, slot, blk, ts, dsm, rec);
+    rows_sum<BF16>(CV, Ycond, out, ts.tok((int32_t)threadIdx.x / kLanes), tr, dsm, rec);
 }
 
 }  // namespace tdp_cr

@@ -280,27 +280,33 @@ tdp_status tdp_cond_blend(tdp_plan_t plan, int32_t N, int32_t ncap, const void *
  * ("Shared negative (reference) positions": a token kept by several tiles has blend weight
  *  1/(number of tiles that kept it).)
  *
- * tdp_cond_records, once: for every block of 8 consecutive tokens of a batch item, its
- * record: the rows of Ycond its tokens sum (each token's in ascending tile order), the rows
- * per token and the tiles that kept each token.  The records are stored in launch order,
- * the blocks with the most rows first, so that the longest blocks start first.
+ * tdp_cond_records, once: the B*N tokens dealt to G = B * ceil(N/8) records of 8, so that every
+ * record holds about as many rows of Ycond: tokens ranked by class of stored rows (16 classes
+ * of ceil((n_tiles + 1) / 16) rows, most rows first, ties in token order), rank r at place
+ * r / G of record r % G in even rounds and of record G - 1 - r % G in odd ones.  Each
+ * record holds its tokens, the rows of Ycond they sum (each token's in ascending tile
+ * order), the rows per token and the tiles that kept each token.
  * tdp_cond_blend_records, each call: out as tdp_cond_blend writes it, bit for bit, from the
- * records instead of the slots.
+ * records instead of the slots (each token sums its own rows, wherever it is dealt).
  *
  *   N, ncap, slot   as for tdp_cond_blend (slot from tdp_norm_filter or tdp_split_filter).
  *   recs            device int32, tdp_cond_records_size(plan, N) ints, 16-byte aligned; written
- *                   by tdp_cond_records, read by tdp_cond_blend_records.  Layout: G = B *
- *                   ceil(N/8) records of rec = ceil4(18 + 8 * n_tiles) ints each, the i-th
- *                   launched i-th ([0] token block g = b * ceil(N/8) + k0/8, [1] its rows R,
- *                   [2..10) rows per token, [10..18) tiles that kept each token, [18..18+R)
- *                   row numbers (t*B + b)*ncap + slot of Ycond), then G ints: each token
- *                   block's launch position.
+ *                   by tdp_cond_records, read by tdp_cond_blend_records.  Layout: G records of
+ *                   rec = ceil4(26 + 8 * n_tiles) ints each ([0] its number, [1] its rows R,
+ *                   [2..10) rows per token, [10..18) tiles that kept each token, [18..26) each
+ *                   token's index b*N + k, or -1 for an empty place, [26..26+R) row numbers
+ *                   (t*B + b)*ncap + slot of Ycond), then the deal (8*G ints, record after
+ *                   record, token index or -1), then every token's info (8*G ints, the first
+ *                   B*N used: tiles that kept it << 16 | rows stored), then every token's
+ *                   stored rows in ascending tile order (B*N lists, n_tiles ints apart),
+ *                   then 32 * ceil(B*N/32) + 16 ints of the deal's tables (class counts and
+ *                   first ranks per 32 tokens, class offsets).
  *   Ycond, out      as for tdp_cond_blend, with the ncap the records were made with.
  * Records made for one plan, N, ncap and slot are valid only for those; a buffer that does
  * not hold them gives wrong outputs, but tdp_cond_blend_records reads no row of Ycond
- * numbered n_tiles*B*ncap or more and writes no token outside [B, N).  At most 256 tiles
- * (TDP_ERR_TOO_LARGE beyond; tdp_cond_blend takes any count).  tdp_cond_records runs three
- * kernels; tdp_cond_blend_records one.
+ * numbered n_tiles*B*ncap or more and writes no token outside [B, N).  At most 256 tiles and
+ * B*ceil(N/8)*8 below 2^31 (TDP_ERR_TOO_LARGE beyond; tdp_cond_blend takes any count).
+ * tdp_cond_records runs four kernels; tdp_cond_blend_records one.
  */
 tdp_status tdp_cond_records_size(tdp_plan_t plan, int32_t N, int64_t *ints);
 tdp_status tdp_cond_records(tdp_plan_t plan, int32_t N, int32_t ncap, const int32_t *slot, int32_t *recs,

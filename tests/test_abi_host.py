@@ -225,9 +225,10 @@ def test_threads_share_a_plan_and_keep_their_own_error_detail(tdp):
 
 
 def test_cond_records_size_and_refusals(tdp):
-    """The records' size follows the documented layout (G records of ceil4(18 + 8 nt) ints,
-    then G positions); shapes the records do not take, and bad arguments, are refused on the
-    host."""
+    """The records' size follows the documented layout (G records of ceil4(26 + 8 nt) ints,
+    then the deal, 8 tokens per record, 8 G ints of per-token info, B N nt ints of per-token
+    lists and the deal's tables, 32 ceil(B N / 32) + 16 ints); shapes the records do not take,
+    and bad arguments, are refused on the host."""
     lib = ctypes.CDLL(tdp.LIB_PATH)
     vp, i32 = ctypes.c_void_p, ctypes.c_int32
     lib.tdp_cond_records_size.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_int64)]
@@ -236,8 +237,10 @@ def test_cond_records_size_and_refusals(tdp):
     for wl in wk.WORKLOADS:
         plan = tdp.tdp_plan_create(wl.B, wl.F, wl.H, wl.W, wl.C, wl.dtype, wl.num_tiles, wl.overlap)
         G = wl.B * ((wl.n_cond + 7) // 8)
-        rec = (18 + 8 * plan.n_tiles + 3) // 4 * 4
-        assert tdp.tdp_cond_records_size(plan, wl.n_cond) == G * rec + G
+        rec = (26 + 8 * plan.n_tiles + 3) // 4 * 4
+        P = (wl.B * wl.n_cond + 31) // 32
+        assert tdp.tdp_cond_records_size(plan, wl.n_cond) == \
+            G * rec + 16 * G + wl.B * wl.n_cond * plan.n_tiles + 32 * P + 16
     plan = tdp.tdp_plan_create(1, 3, 8, 12, 16, "f32", (1, 2, 2), (0, 2, 2))
     n = ctypes.c_int64(-1)
     assert lib.tdp_cond_records_size(plan.handle, 0, ctypes.byref(n)) == 0 and n.value == 0

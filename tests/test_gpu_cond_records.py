@@ -1,8 +1,8 @@
 """tdp_cond_records + tdp_cond_blend_records, the conditioning-token output reduction in two
 calls ("Tiled Data Parallelism (TDP)", "Shared negative (reference) positions": weight
 1/(tiles that kept it)): the outputs are bit for bit those of tdp_cond_blend, which the
-reduction tests compare with the CPU oracle; the records themselves are checked against the
-filter's slots and counts."""
+reduction tests compare with the CPU oracle; the records themselves, and the deal of the
+tokens to them, are checked against the filter's slots and counts."""
 import numpy as np
 import pytest
 
@@ -13,8 +13,8 @@ from gpu_path import assert_blend_close, fill_sentinel, run_split_filter, to_dev
 pytestmark = pytest.mark.gpu
 
 TOK = 8          # tokens per block
-HEAD = 2 + 2 * TOK
-STAGE_ROWS = 48  # rows per stage of the row ring: blocks are launched by stages filled, most first
+HEAD = 2 + 3 * TOK
+CLASSES = 16     # classes of stored rows the deal ranks tokens by
 
 
 @pytest.fixture(scope="module")
@@ -63,38 +63,52 @@ def _same(a, b):
 
 
 def _check_records(plan, wl, out, N, ncap, recs):
-    """Every token block has one record, at its launch position; the records list the rows of
-    the filter's slots in ascending tile order, and the launch order is by stages filled."""
+    """The deal: tokens ranked by class min(rows // width, 15) of their stored rows, classes in
+    descending order and tokens of a class in ascending order, rank r at place r // G of record
+    r % G (rounds alternate direction); every token once.  Every token's info (tiles that kept
+    it, stored rows) and, on a sample, its list.  Record i: its tokens, their stored rows in
+    ascending tile order, the rows per token and the tiles that kept each token."""
     B, nt = wl.B, plan.n_tiles
-    nkb = (N + TOK - 1) // TOK
-    G = B * nkb
+    G = B * ((N + TOK - 1) // TOK)
     stride = (HEAD + TOK * nt + 3) // 4 * 4
     r = recs.cpu().numpy()
-    pos = r[G * stride:]
-    assert sorted(pos.tolist()) == list(range(G))
     slot = out["slot"]                                     # [nt, B, N]
     kcount = out["kcount"]                                 # [B, N]
-    classes = []
-    for g in range(G):
-        rec = r[pos[g] * stride:(pos[g] + 1) * stride]
-        assert rec[0] == g
-        b, k0 = divmod(g, nkb)
-        k0 *= TOK
+    stored = (slot >= 0) & (slot < ncap)
+    lens = stored.sum(0).reshape(-1)                       # token b N + k
+    width = (nt + CLASSES) // CLASSES
+    cls = np.minimum(lens // width, CLASSES - 1)
+    order = np.argsort(-cls, kind="stable")
+    want = np.full((G, TOK), -1, np.int64)
+    for rank, tok in enumerate(order):
+        q, p = divmod(rank, G)
+        want[G - 1 - p if q % 2 else p, q] = tok
+    assign = r[G * stride:G * stride + G * TOK].reshape(G, TOK)
+    assert np.array_equal(assign, want), "the deal differs"
+    info = r[G * stride + G * TOK:G * stride + G * TOK + B * N]
+    assert np.array_equal(info & 0xffff, lens) and np.array_equal(info >> 16, kcount.reshape(-1))
+    lists = r[G * stride + 2 * G * TOK:].view(np.uint32)
+    for tok in range(0, B * N, max(1, B * N // 64)):
+        b, k = divmod(tok, N)
+        mine = [(t * B + b) * ncap + slot[t, b, k] for t in range(nt) if stored[t, b, k]]
+        assert lists[tok * nt:tok * nt + len(mine)].tolist() == mine
+    for i in range(G):
+        rec = r[i * stride:(i + 1) * stride]
+        assert rec[0] == i
         rows = []
         for j in range(TOK):
-            k = k0 + j
-            if k < N:
-                stored = [(t * B + b) * ncap + slot[t, b, k] for t in range(nt) if 0 <= slot[t, b, k] < ncap]
-                assert rec[2 + j] == len(stored) and rec[2 + TOK + j] == kcount[b, k]
+            tok = int(want[i, j])
+            assert rec[2 + 2 * TOK + j] == tok
+            if tok >= 0:
+                b, k = divmod(tok, N)
+                mine = [(t * B + b) * ncap + slot[t, b, k] for t in range(nt) if stored[t, b, k]]
+                assert rec[2 + j] == len(mine) and rec[2 + TOK + j] == kcount[b, k]
             else:
-                stored = []
+                mine = []
                 assert rec[2 + j] == 0 and rec[2 + TOK + j] == 0
-            rows += stored
+            rows += mine
         assert rec[1] == len(rows)
         assert rec[HEAD:HEAD + len(rows)].astype(np.uint32).tolist() == rows
-        classes.append((pos[g], min(7, (len(rows) + STAGE_ROWS - 1) // STAGE_ROWS)))
-    order = [c for _, c in sorted(classes)]
-    assert order == sorted(order, reverse=True), "launch order is not by stages filled, most first"
 
 
 @pytest.mark.parametrize("name", ["tiny", "small", "medium", "temporal", "large"])
@@ -186,7 +200,7 @@ def test_foreign_records_stay_in_bounds(tdp):
     tdp.tdp_cond_blend_records(plan, N, recs, Yc, ncap, big[pad:pad + wl.B * N * wl.C])
     torch.cuda.synchronize()
     assert _same(big[:pad], ref[:pad]) and _same(big[-pad:], ref[-pad:])
-    # the same buffer with plausible block numbers: every record's block in [0, G)
+    # the same buffer with plausible block numbers: every record's number in [0, G)
     G = wl.B * ((N + TOK - 1) // TOK)
     stride = (HEAD + TOK * plan.n_tiles + 3) // 4 * 4
     r = recs[:G * stride].view(G, stride)
