@@ -331,22 +331,12 @@ extern "C" tdp_status tdp_cond_blend_records(tdp_plan_t plan, int32_t N, int32_t
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const uint4 *y = reinterpret_cast<const uint4 *>(Ycond);
     uint4 *o = reinterpret_cast<uint4 *>(out);
-    cudaError_t err;
-    if (g.nt >= kRecRowsTiles) {
-        const size_t smem = rows_layout(g.nt, kRecRows).bytes;
-        err = g.dtype == TDP_BF16
-                  ? tdp_launch_smem(true, tdp_cond_blend_rec_kernel<1, kRecRows>, (unsigned)G, kTokThreads, smem, s,
-                                    g.nt, (int64_t)g.B * N, (uint32_t)nrows, CV, recs, y, o)
-                  : tdp_launch_smem(true, tdp_cond_blend_rec_kernel<0, kRecRows>, (unsigned)G, kTokThreads, smem, s,
-                                    g.nt, (int64_t)g.B * N, (uint32_t)nrows, CV, recs, y, o);
-    } else {
-        const size_t smem = rows_layout(g.nt).bytes;
-        err = g.dtype == TDP_BF16
-                  ? tdp_launch_smem(true, tdp_cond_blend_rec_kernel<1, kChunkRows>, (unsigned)G, kTokThreads, smem, s,
-                                    g.nt, (int64_t)g.B * N, (uint32_t)nrows, CV, recs, y, o)
-                  : tdp_launch_smem(true, tdp_cond_blend_rec_kernel<0, kChunkRows>, (unsigned)G, kTokThreads, smem, s,
-                                    g.nt, (int64_t)g.B * N, (uint32_t)nrows, CV, recs, y, o);
-    }
+    const size_t smem = rows_layout(g.nt).bytes;
+    cudaError_t err = g.dtype == TDP_BF16
+                          ? tdp_launch_smem(true, tdp_cond_blend_rec_kernel<1, kChunkRows>, (unsigned)G, kTokThreads,
+                                            smem, s, g.nt, (int64_t)g.B * N, (uint32_t)nrows, CV, recs, y, o)
+                          : tdp_launch_smem(true, tdp_cond_blend_rec_kernel<0, kChunkRows>, (unsigned)G, kTokThreads,
+                                            smem, s, g.nt, (int64_t)g.B * N, (uint32_t)nrows, CV, recs, y, o);
     if (err == cudaSuccess) err = cudaGetLastError();
     if (err != cudaSuccess) return tdp_fail(TDP_ERR_CUDA, cudaGetErrorString(err));
     return tdp_ok();

@@ -31,7 +31,7 @@ constexpr int kTokThreads = 128;  // threads per token block
 constexpr int kTok = 8;           // tokens per block: a half-warp each
 constexpr int kLanes = 16;        // lanes per token: channel vectors per slab
 constexpr int kTokMinBlocks = 8;  // resident blocks per SM the token kernel is compiled for
-constexpr int kChunkRows = 48;    // rows per stage of the ring (the slot path's ring)
+constexpr int kChunkRows = 48;    // rows per stage of the ring
 constexpr int kStages = 2;        // stages of the ring
 static_assert(kTokThreads == kTok * kLanes, "a half-warp per token");
 static_assert((kChunkRows * kLanes) % kTokThreads == 0, "the copies of a stage split evenly over the block");
@@ -39,10 +39,6 @@ static_assert((kChunkRows * kLanes) % kTokThreads == 0, "the copies of a stage s
 // Bytes of a ring of kStages stages of CR rows.
 __host__ __device__ constexpr size_t ring_bytes(int CR) { return (size_t)kStages * CR * kLanes * 16; }
 
-// The records path (tdp_cond_records) runs its blocks with stages of kRecRows rows on plans of
-// kRecRowsTiles tiles or more, where tokens hold more rows, else of kChunkRows.
-constexpr int kRecRows = 64;
-constexpr int kRecRowsTiles = 64;
 
 // a += y, 4 fp32 or 8 bf16 values; a bf16 value is added to its fp32 sum in one
 // mixed-precision add (the bf16 value widened exactly, the sum rounded to nearest).
