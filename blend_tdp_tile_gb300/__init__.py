@@ -407,8 +407,9 @@ def tdp_cond_records_size(plan: Plan, N) -> int:
 
 
 def tdp_cond_records(plan: Plan, N, ncap, slot, recs, stream=None):
-    """Once per set of conditioning tokens: every token block's record (rows and weights), in
-    launch order, into recs (int32, tdp_cond_records_size elements)."""
+    """Once per set of conditioning tokens: the tokens dealt to records of 8 by stored rows, and
+    every record (its tokens, their rows and weights), into recs (int32,
+    tdp_cond_records_size elements)."""
     torch = _torch()
     B, nt, N, ncap = plan.B, plan.n_tiles, int(N), int(ncap)
     c = _Call("tdp_cond_records")
