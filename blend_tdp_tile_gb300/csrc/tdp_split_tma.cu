@@ -148,8 +148,8 @@ __device__ __forceinline__ unit_id unit_of(const tdp_geom &g, int64_t u)
 
 // Positions of one latent row (b, f, h) by one warp.  The warp first lists, in its table
 // in shared memory, where the row starts in each tile holding it (per F/H combo and
-// W-tile: the position-buffer index of cell w = 0, the tile's token count and its (tile,
-// batch) row of mn); its lanes then stride over the row's 3*W [start, end) pairs,
+// W-tile: the position-buffer index of cell w = 0, the tile's token count and, when
+// normalising, the tile's mn); its lanes then stride over the row's 3*W [start, end) pairs,
 // kPosBatch loads in flight each, and store every pair, minus the tile's mn when
 // normalising, to each tile holding it (at most 2 x 2 x 2).
 constexpr int kPosBatch = 4;
@@ -157,7 +157,8 @@ constexpr int kPosBatch = 4;
 struct pos_entry {
     int64_t qpos;          // index of (d = 0, cell w = 0) of the row in the tile's positions
     int64_t Tt;            // tokens of the tile
-    int32_t tb, pad;       // t * B + b
+    int32_t sub[3];        // what each dimension's pairs lose: the tile's mn, or 0
+    int32_t pad;
 };
 
 __device__ __forceinline__ void split_pos_row(const tdp_geom &g, int64_t row, const int2 *__restrict__ P,
@@ -168,6 +169,22 @@ __device__ __forceinline__ void split_pos_row(const tdp_geom &g, int64_t row, co
     const int32_t h = (int32_t)(row % g.H), f = (int32_t)((row / g.H) % g.F);
     const int32_t b = (int32_t)(row / ((int64_t)g.H * g.F));
     const tdp_row_combos rc = tdp_make_combos(g, f, h);
+    const int64_t T = (int64_t)g.F * g.H * g.W;
+    const int2 *src = P + (int64_t)b * 3 * T + ((int64_t)f * g.H + h) * g.W;
+    const int32_t n = 3 * g.W;
+    // the first pairs' loads in flight while the table is built
+    int2 p[kPosBatch];
+    auto load = [&](int32_t q0) {
+#pragma unroll
+        for (int u = 0; u < kPosBatch; ++u) {
+            const int32_t q = q0 + 32 * u;
+            if (q < n) {
+                const int32_t d = q / g.W;
+                p[u] = __ldcs(src + (int64_t)d * T + (q - d * g.W));
+            }
+        }
+    };
+    load(lane);
     __syncwarp();                                     // the previous row's table is no longer read
     for (int32_t e = lane; e < rc.nc * nW; e += 32) {
         const int32_t c = e / nW, iW = e - c * nW;
@@ -179,24 +196,15 @@ __device__ __forceinline__ void split_pos_row(const tdp_geom &g, int64_t row, co
         pe.Tt = SF * SH * SW;
         pe.qpos = (int64_t)g.B * tdp_tile_off(g, iF, iH, iW) * 3 + (int64_t)b * 3 * pe.Tt +
                   ((int64_t)(f - g.d[0].lo[iF]) * SH + (h - g.d[1].lo[iH])) * SW - g.d[2].lo[iW];
-        pe.tb = ((iF * g.d[1].n + iH) * nW + iW) * g.B + b;
+        const int32_t tb = ((iF * g.d[1].n + iH) * nW + iW) * g.B + b;
+#pragma unroll
+        for (int d = 0; d < 3; ++d) pe.sub[d] = normalize ? __ldg(mn + (int64_t)tb * 3 + d) : 0;
         pe.pad = 0;
         tab[e] = pe;
     }
     __syncwarp();
-    const int64_t T = (int64_t)g.F * g.H * g.W;
-    const int2 *src = P + (int64_t)b * 3 * T + ((int64_t)f * g.H + h) * g.W;
-    const int32_t n = 3 * g.W;
     for (int32_t q0 = lane; q0 < n; q0 += 32 * kPosBatch) {
-        int2 p[kPosBatch];
-#pragma unroll
-        for (int u = 0; u < kPosBatch; ++u) {
-            const int32_t q = q0 + 32 * u;
-            if (q < n) {
-                const int32_t d = q / g.W;
-                p[u] = __ldcs(src + (int64_t)d * T + (q - d * g.W));
-            }
-        }
+        if (q0 != lane) load(q0);
 #pragma unroll
         for (int u = 0; u < kPosBatch; ++u) {
             const int32_t q = q0 + 32 * u;
@@ -208,13 +216,9 @@ __device__ __forceinline__ void split_pos_row(const tdp_geom &g, int64_t row, co
                 for (int32_t k = 0; k < 2; ++k) {
                     const int32_t iW = k ? w1 : w0;
                     if (iW < 0) break;
-                    const pos_entry pe = tab[c * nW + iW];
-                    int2 o = p[u];
-                    if (normalize) {
-                        const int32_t m = __ldg(mn + (int64_t)pe.tb * 3 + d);
-                        o.x = (int32_t)((uint32_t)o.x - (uint32_t)m);
-                        o.y = (int32_t)((uint32_t)o.y - (uint32_t)m);
-                    }
+                    const pos_entry &pe = tab[c * nW + iW];
+                    const uint32_t m = (uint32_t)pe.sub[d];
+                    const int2 o = make_int2((int32_t)((uint32_t)p[u].x - m), (int32_t)((uint32_t)p[u].y - m));
                     Q[pe.qpos + (int64_t)d * pe.Tt + w] = o;
                 }
             }
