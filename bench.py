@@ -862,6 +862,12 @@ def run_ours(args, rank, world, local_rank):
                           for k, v in calls.items()},
                 "latent_tokens_per_s": calls["step"]["latent_tokens_per_s"],
             }
+            if fl is not None:
+                # the same calls without the flush: launches back to back on inputs left in L2
+                warm = time_calls(c, torch, peak)
+                per_workload[w.name]["calls_without_flush"] = {
+                    "note": "no flush between launches: inputs resident in L2, not an HBM measurement",
+                    **{k: {"ms": v["ms"], "GB/s": v["GB/s"]} for k, v in warm.items()}}
             if c is not case:
                 del c
                 torch.cuda.empty_cache()
