@@ -25,73 +25,20 @@ tdp_blend_kernel(const __grid_constant__ tdp_geom g, int32_t cv_shift, const uin
 
 // ---------------------------------------------------------------------------
 // Partial blend for round-robin ranks ("What it is": tiles go to ranks round-robin and
-// one all_reduce sums the ranks' blended tiles).  Block = one latent row (b, f, h); a
-// thread takes one 16-byte input vector of a cell at a time, loads the covering tiles
-// that rank `rank` owns (t % world == rank; at most 8, all loads in flight before the
-// arithmetic) and writes their mask-weighted sum in fp32, in ascending t with the same
-// operations as tdp_blend_kernel, or +0 where the rank owns no covering tile.  With
-// world == 1 the sums are tdp_blend_kernel's before its final rounding.
+// one all_reduce sums the ranks' blended tiles).  Block = one latent row (b, f, h), the
+// blend's row routine in its partial mode: the loads of the covering tiles rank `rank`
+// owns (t % world == rank) go through the same shared-memory slots, and each output is
+// their mask-weighted sum in fp32, in ascending t with tdp_blend_kernel's operations, or
+// +0 where the rank owns no covering tile.  With world == 1 the sums are tdp_blend_kernel's
+// before its final rounding.
 // ---------------------------------------------------------------------------
-constexpr int kPartialThreads = 128;
-
 template <int BF16>
-__global__ void __launch_bounds__(kPartialThreads)
-tdp_blend_partial_kernel(const __grid_constant__ tdp_geom g, int32_t rank, int32_t world,
+__global__ void __launch_bounds__(kBlendThreads, kBlendMinBlocks)
+tdp_blend_partial_kernel(const __grid_constant__ tdp_geom g, int32_t cv_shift, int32_t rank, int32_t world,
                          const uint4 *__restrict__ Yout, float4 *__restrict__ Zp)
 {
-    using VM = vec_math<BF16>;
-    constexpr int kE = VM::kElems;                    // elements per 16-byte input vector
-    __shared__ int64_t s_tok[TDP_MAX_COMBOS * TDP_MAX_TILES_PER_DIM];
-    __shared__ int32_t s_loW[TDP_MAX_TILES_PER_DIM], s_hiW[TDP_MAX_TILES_PER_DIM];
-    tdp_pdl_trigger();
-    for (int32_t i = threadIdx.x; i < g.d[2].n; i += blockDim.x) {
-        s_loW[i] = g.d[2].lo[i];
-        s_hiW[i] = g.d[2].hi[i];
-    }
-    const int32_t row = blockIdx.x;
-    const int32_t h = row % g.H, f = (row / g.H) % g.F, b = row / (g.H * g.F);
-    const tdp_row_combos rc = tdp_make_combos(g, f, h);
-    tdp_fill_row_table(g, rc, b, f, h, s_tok, nullptr, nullptr, nullptr);   // ends with a barrier
-    const int32_t nW = g.d[2].n, nH = g.d[1].n, oW = g.d[2].o;
-    const int32_t CV = (g.C * g.esize) >> 4;
-    const int64_t T = (int64_t)g.F * g.H * g.W;
-    tdp_pdl_wait();
-    const int64_t zrow = ((int64_t)b * T + ((int64_t)f * g.H + h) * g.W) * CV;   // first input vector of the row
-    const int32_t nvec = g.W * CV;
-    for (int32_t v = threadIdx.x; v < nvec; v += blockDim.x) {
-        const int32_t w = v / CV, cv = v - w * CV;
-        const tdp_cover cW = tdp_cover_tab(s_loW, s_hiW, nW, g.W, oW, w);
-        const float r0 = tdp_weight(cW.num0, oW), r1 = tdp_weight(cW.num1, oW);
-        uint4 y[TDP_MAX_COMBOS][2];
-        bool own[TDP_MAX_COMBOS][2];
-#pragma unroll
-        for (int c = 0; c < TDP_MAX_COMBOS; ++c)
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                const int32_t iW = k ? cW.i1 : cW.i0;
-                const int32_t t = c < rc.nc && iW >= 0 ? (rc.iF(c) * nH + rc.iH(c)) * nW + iW : -1;
-                own[c][k] = t >= 0 && t % world == rank;
-                if (own[c][k]) y[c][k] = __ldcs(Yout + (s_tok[c * nW + iW] + w) * CV + cv);
-            }
-        float acc[kE];
-#pragma unroll
-        for (int e = 0; e < kE; ++e) acc[e] = 0.0f;
-        bool first = true;
-#pragma unroll
-        for (int c = 0; c < TDP_MAX_COMBOS; ++c)
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                if (!own[c][k]) continue;
-                const float m = rc.rFH(c) * (k ? r1 : r0);
-                if (first) VM::mul(acc, m, y[c][k]);           // the first term keeps the sign of zero
-                else VM::fma(acc, m, y[c][k]);
-                first = false;
-            }
-        float4 *dst = Zp + (zrow + v) * (kE / 4);
-#pragma unroll
-        for (int q = 0; q < kE / 4; ++q)
-            __stcs(dst + q, make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]));
-    }
+    extern __shared__ __align__(16) unsigned char dsm[];
+    blend_row<BF16, 1>(g, cv_shift, Yout, Zp, blockIdx.x, dsm, rank, world);
 }
 
 // Z[i] = Zsum[i] in the plan's dtype (round to nearest even for bf16): 8 (bf16) or 4 (fp32)
@@ -119,12 +66,12 @@ tdp_blend_store_kernel(int64_t nvec, const float4 *__restrict__ Zsum, uint4 *__r
 }
 
 // Raise `kernel`'s dynamic shared-memory limit to `bytes` once per device (calls after the
-// first with a given size make no attribute change).
+// first with a given size make no attribute change); `which` names the kernel (0, 1: the
+// blend in f32, bf16; 2, 3: the partial blend).
 template <typename K>
-cudaError_t allow_blend_smem(K kernel, size_t bytes)
+cudaError_t allow_blend_smem(K kernel, int which, size_t bytes)
 {
-    static std::atomic<int> raised[2][64];
-    const int which = kernel == reinterpret_cast<K>(tdp_blend_kernel<1>) ? 1 : 0;
+    static std::atomic<int> raised[4][64];
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
@@ -151,12 +98,20 @@ extern "C" tdp_status tdp_blend_partial(tdp_plan_t plan, int32_t rank, int32_t w
     if (!tdp_aligned(Yout, 16) || !tdp_aligned(Zp, 16))
         return tdp_fail(TDP_ERR_MISALIGNED, "Yout and Zp must be 16-byte aligned");
     const unsigned rows = (unsigned)((int64_t)g.B * g.F * g.H);
+    const int32_t CV = (g.C * g.esize) >> 4;
+    const int32_t cv_shift = (CV & (CV - 1)) == 0 ? __builtin_ctz((unsigned)CV) : -1;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const uint4 *y = reinterpret_cast<const uint4 *>(Yout);
     float4 *z = reinterpret_cast<float4 *>(Zp);
-    cudaError_t err = g.dtype == TDP_BF16
-                          ? tdp_launch(true, tdp_blend_partial_kernel<1>, rows, kPartialThreads, s, g, rank, world, y, z)
-                          : tdp_launch(true, tdp_blend_partial_kernel<0>, rows, kPartialThreads, s, g, rank, world, y, z);
+    const size_t wsmem = blend_smem(g);
+    cudaError_t err = g.dtype == TDP_BF16 ? allow_blend_smem(tdp_blend_partial_kernel<1>, 3, wsmem)
+                                          : allow_blend_smem(tdp_blend_partial_kernel<0>, 2, wsmem);
+    if (err == cudaSuccess)
+        err = g.dtype == TDP_BF16
+                  ? tdp_launch_smem(true, tdp_blend_partial_kernel<1>, rows, kBlendThreads, wsmem, s, g, cv_shift, rank,
+                                    world, y, z)
+                  : tdp_launch_smem(true, tdp_blend_partial_kernel<0>, rows, kBlendThreads, wsmem, s, g, cv_shift, rank,
+                                    world, y, z);
     if (err == cudaSuccess) err = cudaGetLastError();
     if (err != cudaSuccess) return tdp_fail(TDP_ERR_CUDA, cudaGetErrorString(err));
     return tdp_ok();
@@ -202,7 +157,8 @@ extern "C" tdp_status tdp_blend(tdp_plan_t plan, const void *Yout, void *Z, tdp_
     // the W-cell table is sized to the row (up to kWTab cells), so that short rows leave
     // room for more blocks per SM
     const size_t wsmem = blend_smem(g);
-    cudaError_t err = g.dtype == TDP_BF16 ? allow_blend_smem(tdp_blend_kernel<1>, wsmem) : allow_blend_smem(tdp_blend_kernel<0>, wsmem);
+    cudaError_t err = g.dtype == TDP_BF16 ? allow_blend_smem(tdp_blend_kernel<1>, 1, wsmem)
+                                          : allow_blend_smem(tdp_blend_kernel<0>, 0, wsmem);
     if (err == cudaSuccess)
         err = g.dtype == TDP_BF16
                   ? tdp_launch_smem(true, tdp_blend_kernel<1>, rows, kBlendThreads, wsmem, s, g, cv_shift, y, z)

@@ -101,10 +101,14 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 
 // One latent row of the blend, by the whole block (blend_smem(g) bytes of dynamic shared
 // memory at dsm).  Waits for the work before it in the stream (griddepcontrol.wait)
-// before it reads Yout.
-template <int BF16>
+// before it reads Yout.  PART = 0: Z holds the latent in the plan's dtype.  PART = 1, the
+// round-robin partial: only the tiles t with t % world == rank are loaded and summed (the
+// first of them multiplied, the others added, in the same order; +0 where the rank owns no
+// covering tile), and Z holds fp32 (kElems floats per 16-byte input vector).
+template <int BF16, int PART = 0>
 __device__ __forceinline__ void blend_row(const tdp_geom &g, int32_t cv_shift, const uint4 *__restrict__ Yout,
-                                          uint4 *__restrict__ Z, int32_t row, unsigned char *dsm)
+                                          void *__restrict__ Zv, int32_t row, unsigned char *dsm, int32_t rank = 0,
+                                          int32_t world = 1)
 {
     using VM = vec_math<BF16>;
     __shared__ int64_t s_tok[TDP_MAX_COMBOS * TDP_MAX_TILES_PER_DIM];
@@ -131,6 +135,18 @@ __device__ __forceinline__ void blend_row(const tdp_geom &g, int32_t cv_shift, c
     // sits at Yout + s_tok[c * nW + iW] + w * CV + cv
     for (int32_t e = threadIdx.x; e < rc.nc * nW; e += blockDim.x) s_tok[e] *= CV;
     const int32_t nc = rc.nc;
+    // PART: which of the row's (combo, W-tile) tiles this rank owns
+    uint8_t *s_own = nullptr;
+    if constexpr (PART != 0) {
+        __shared__ uint8_t own_tab[TDP_MAX_COMBOS * TDP_MAX_TILES_PER_DIM];
+        s_own = own_tab;
+        for (int32_t e = threadIdx.x; e < nc * nW; e += blockDim.x) {
+            const int32_t c = e / nW, iW = e - c * nW;
+            const int32_t t = (rc.iF(c) * g.d[1].n + rc.iH(c)) * nW + iW;
+            own_tab[e] = t % world == rank ? 1 : 0;
+        }
+        __syncthreads();
+    }
     float rFH[TDP_MAX_COMBOS];
 #pragma unroll
     for (int c = 0; c < TDP_MAX_COMBOS; ++c) rFH[c] = c < nc ? rc.rFH(c) : 0.0f;
@@ -151,7 +167,7 @@ __device__ __forceinline__ void blend_row(const tdp_geom &g, int32_t cv_shift, c
         __syncthreads();
         // vector v of this pass is cell wbase + v / CV: at ybase + tile offset + v
         const uint4 *ybase = Yout + (int64_t)wbase * CV;
-        uint4 *zbase = Z + ((int64_t)b * T + ((int64_t)f * g.H + h) * g.W + wbase) * CV;
+        const int64_t zoff = ((int64_t)b * T + ((int64_t)f * g.H + h) * g.W + wbase) * CV;   // output vectors
         const int32_t nvec = wn * CV;
         // Eight load slots per pass, copied global -> shared memory with cp.async (no
         // registers held while in flight), two passes' slots per thread: a thread issues
@@ -168,9 +184,9 @@ __device__ __forceinline__ void blend_row(const tdp_geom &g, int32_t cv_shift, c
                 if (v < nvec) {
                     const int32_t iw = s_w[cv_shift >= 0 ? (v >> cv_shift) : v / CV].iw;
                     const int32_t iWx = (sl & 1) ? (iw >> 16) - 1 : (iw & 0xffff);
-                    if (iWx >= 0)
-                        cp_async16(stage + ((buf * 8 + sl) * kBlendThreads + threadIdx.x) * 16u,
-                                   ybase + s_tok[((sl >> 1) & (nc - 1)) * nW + iWx] + v);
+                    const int32_t ce = ((sl >> 1) & (nc - 1)) * nW + iWx;
+                    if (iWx >= 0 && (PART == 0 || s_own[ce]))
+                        cp_async16(stage + ((buf * 8 + sl) * kBlendThreads + threadIdx.x) * 16u, ybase + s_tok[ce] + v);
                 }
             }
             cp_async_commit();
@@ -193,16 +209,44 @@ __device__ __forceinline__ void blend_row(const tdp_geom &g, int32_t cv_shift, c
                 const bool two = (e.iw >> 16) != 0;
                 const int32_t s0 = q << lq;
                 float acc[VM::kElems];
-                VM::mul(acc, rFH[0] * e.r0, sb[s0 * kBlendThreads]);          // the first term keeps the sign of zero
-                if (two) VM::fma(acc, rFH[0] * e.r1, sb[(s0 + 1) * kBlendThreads]);
+                if constexpr (PART == 0) {
+                    VM::mul(acc, rFH[0] * e.r0, sb[s0 * kBlendThreads]);          // the first term keeps the sign of zero
+                    if (two) VM::fma(acc, rFH[0] * e.r1, sb[(s0 + 1) * kBlendThreads]);
 #pragma unroll
-                for (int c = 1; c < TDP_MAX_COMBOS; ++c) {
-                    if (c < nc) {
-                        VM::fma(acc, rFH[c] * e.r0, sb[(s0 + 2 * c) * kBlendThreads]);
-                        if (two) VM::fma(acc, rFH[c] * e.r1, sb[(s0 + 2 * c + 1) * kBlendThreads]);
+                    for (int c = 1; c < TDP_MAX_COMBOS; ++c) {
+                        if (c < nc) {
+                            VM::fma(acc, rFH[c] * e.r0, sb[(s0 + 2 * c) * kBlendThreads]);
+                            if (two) VM::fma(acc, rFH[c] * e.r1, sb[(s0 + 2 * c + 1) * kBlendThreads]);
+                        }
                     }
+                    __stcs(reinterpret_cast<uint4 *>(Zv) + zoff + v, VM::pack(acc));
+                } else {
+                    const int32_t iw0 = e.iw & 0xffff, iw1 = (e.iw >> 16) - 1;
+                    bool any = false;
+#pragma unroll
+                    for (int c = 0; c < TDP_MAX_COMBOS; ++c) {
+                        if (c < nc) {
+#pragma unroll
+                            for (int k = 0; k < 2; ++k) {
+                                if (k == 1 && !two) break;
+                                if (!s_own[c * nW + (k ? iw1 : iw0)]) continue;
+                                const float m = rFH[c] * (k ? e.r1 : e.r0);
+                                const uint4 &y = sb[(s0 + 2 * c + k) * kBlendThreads];
+                                if (!any) VM::mul(acc, m, y);                     // the first owned term
+                                else VM::fma(acc, m, y);
+                                any = true;
+                            }
+                        }
+                    }
+                    if (!any) {
+#pragma unroll
+                        for (int x = 0; x < VM::kElems; ++x) acc[x] = 0.0f;
+                    }
+                    float4 *dst = reinterpret_cast<float4 *>(Zv) + (zoff + v) * (VM::kElems / 4);
+#pragma unroll
+                    for (int x = 0; x < VM::kElems / 4; ++x)
+                        __stcs(dst + x, make_float4(acc[4 * x], acc[4 * x + 1], acc[4 * x + 2], acc[4 * x + 3]));
                 }
-                __stcs(zbase + v, VM::pack(acc));
             }
         }
         __syncthreads();   // the table is rebuilt for the next cells
