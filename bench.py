@@ -483,9 +483,10 @@ class L2Flush:
 
 
 def call_ms(torch, s, fn, reps=PER_CALL_REPS, flush=None):
-    """Mean device time of one call of `fn` on stream `s`: `reps` launches, each bracketed by
-    CUDA events on `s` (and, with `flush`, each after an L2 flush).  The GPU is kept busy
-    while the host queues them, so host-side launch work never falls inside an interval."""
+    """Mean device time of one call of `fn` on stream `s` (with the median of the same launches
+    as .median): `reps` launches, each bracketed by CUDA events on `s` (and, with `flush`,
+    each after an L2 flush).  The GPU is kept busy while the host queues them, so host-side
+    launch work never falls inside an interval."""
     with torch.cuda.stream(s):
         for _ in range(3):
             fn()
@@ -500,7 +501,17 @@ def call_ms(torch, s, fn, reps=PER_CALL_REPS, flush=None):
             fn()
             a1.record(s)
     s.synchronize()
-    return statistics.mean(a0.elapsed_time(a1) for a0, a1 in ev)
+    times = [a0.elapsed_time(a1) for a0, a1 in ev]
+    return TimedMs(statistics.mean(times), statistics.median(times))
+
+
+class TimedMs(float):
+    """A mean time in ms (the float) that also carries the median of the same launches."""
+
+    def __new__(cls, mean, median):
+        obj = super().__new__(cls, mean)
+        obj.median = median
+        return obj
 
 
 def rotating_ms(torch, s, fns, reps):
@@ -525,8 +536,11 @@ def rotating_ms(torch, s, fns, reps):
 
 def call_entry(t_ms, nbytes, peak):
     gbs = nbytes / (t_ms * 1e-3) / 1e9
-    return {"ms": t_ms, "algorithmic_bytes": nbytes, "GB/s": gbs, "frac": gbs / peak,
-            "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS}
+    e = {"ms": float(t_ms), "algorithmic_bytes": nbytes, "GB/s": gbs, "frac": gbs / peak,
+         "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS}
+    if isinstance(t_ms, TimedMs):
+        e["ms_median"] = t_ms.median
+    return e
 
 
 def time_calls(case, torch, peak, flush=None, reps=PER_CALL_REPS):
@@ -837,7 +851,7 @@ def run_ours(args, rank, world, local_rank):
             "peak_kind": f"{peak_kind} copy bandwidth", "unit": "GB/s", "frac": kern[dom]["frac"],
             "traffic": profiled_traffic(call, wl.name), "algorithmic_bytes_per_launch": kern[dom]["algorithmic_bytes"],
             "frac_of_nominal_8tbs": kern[dom]["frac_of_nominal_8tbs"],
-            "timing": f"mean of {PER_CALL_REPS} launches of the call, CUDA events on its stream"}
+            "timing": f"mean of {PER_CALL_REPS} launches of the call (ms_median beside), CUDA events on its stream"}
 
     # ---- every workload: each call timed the same way; inputs that fit in L2 are
     # flushed out of it before every launch
@@ -857,6 +871,7 @@ def run_ours(args, rank, world, local_rank):
                 "l2": "flushed before every launch" if fl is not None else "inputs larger than L2; no flush",
                 "calls": {k: dict({"ms": v["ms"], "GB/s": v["GB/s"], "frac": v["frac"],
                                    "frac_of_nominal_8tbs": v["frac_of_nominal_8tbs"]},
+                                  **({"ms_median": v["ms_median"]} if "ms_median" in v else {}),
                                   **({"traffic": profiled_traffic("tdp_" + k, w.name)}
                                      if "tdp_" + k in CALL_KERNELS else {}))
                           for k, v in calls.items()},
